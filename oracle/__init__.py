@@ -1,0 +1,214 @@
+"""CPU oracle for DeepSeek V4.1 sparse latent attention -- TEST INFRASTRUCTURE ONLY.
+
+The plain, slow definition of every step on the path, used to check the CUDA library.  Only
+``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline / reference leg may
+import this package; the product path never does.  The arithmetic lives in ``sa_oracle.c``
+(plain C, f64), which shares nothing with the CUDA sources; this module compiles it with gcc on
+first use and marshals numpy arrays through ctypes.
+
+Sources (see the header of ``sa_oracle.c``): the "Module attn" API page of the spark_model
+deepseek_v41_ref docs (precision paragraph, ring-cache paragraph, act_quant_inplace, pow2_ceil,
+sparse_attn, window_topk_idxs) and the "DeepSeek V4.1" Attention.forward / __init__ pages.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# Status codes of the C functions
+OK, BAD_ARG, UNSUPPORTED, BAD_INDEX = 0, 1, 2, 3
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` next to its source (gcc, IEEE arithmetic, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+               "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i64 = ctypes.c_int64
+            lib.or_bf16_round.restype = ctypes.c_uint16
+            lib.or_bf16_round.argtypes = [ctypes.c_double]
+            lib.or_bf16_to_f64.restype = ctypes.c_double
+            lib.or_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.or_e4m3_to_f64.restype = ctypes.c_double
+            lib.or_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.or_e4m3_encode.restype = ctypes.c_uint8
+            lib.or_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.or_pow2_ceil.restype = ctypes.c_float
+            lib.or_pow2_ceil.argtypes = [ctypes.c_float]
+            lib.or_act_quant.restype = ctypes.c_int
+            lib.or_act_quant.argtypes = [P, i64, i64, P, P, P]
+            lib.or_window_idxs.restype = ctypes.c_int
+            lib.or_window_idxs.argtypes = [i64, i64, i64, P, i64]
+            lib.or_ring_write.restype = ctypes.c_int
+            lib.or_ring_write.argtypes = [P, P, i64, i64, i64, i64]
+            for name in ("or_bf16_round_array", "or_e4m3_encode_array", "or_e4m3_decode_array",
+                         "or_pow2_ceil_array"):
+                getattr(lib, name).restype = None
+                getattr(lib, name).argtypes = [P, P, i64]
+            lib.or_sparse_attn.restype = ctypes.c_int
+            lib.or_sparse_attn.argtypes = [P, P, P, P, ctypes.c_int, P, P, ctypes.c_float,
+                                           i64, i64, i64, i64, i64, i64, P, i64, P, P,
+                                           ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# --------------------------------------------------------------------------------------------
+# scalar codecs (vectorised by plain loops over the C scalar functions)
+# --------------------------------------------------------------------------------------------
+
+def _array_call(name, x, in_dtype, out_dtype):
+    lib = _load()
+    a = np.ascontiguousarray(x, dtype=in_dtype)
+    out = np.empty(a.shape, out_dtype)
+    getattr(lib, name)(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def bf16_round(x) -> np.ndarray:
+    """f64 -> bf16 bits (uint16), round to nearest even."""
+    return _array_call("or_bf16_round_array", x, np.float64, np.uint16)
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bits -> exact f64 (the widening is a bit shift, done here in numpy)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """e4m3 byte -> f64 value (NaN for the two NaN codes)."""
+    return _array_call("or_e4m3_decode_array", codes, np.uint8, np.float64)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """f32 -> e4m3 byte, round to nearest even, saturating at +-448."""
+    return _array_call("or_e4m3_encode_array", x, np.float32, np.uint8)
+
+
+def pow2_ceil(v) -> np.ndarray:
+    """2 ** ceil(log2 v) for positive normal f32, from the IEEE fields."""
+    return _array_call("or_pow2_ceil_array", v, np.float32, np.float32)
+
+
+# --------------------------------------------------------------------------------------------
+# the path's operations
+# --------------------------------------------------------------------------------------------
+
+def act_quant(x_bf16: np.ndarray):
+    """Block-32 e4m3 / ue8m0 round trip of bf16 rows.
+
+    ``x_bf16`` is uint16 [..., d] (bf16 bits), d % 32 == 0.  Returns (x_rt bf16 bits [..., d],
+    codes uint8 [..., d], scales uint8 [..., d/32])."""
+    lib = _load()
+    x = _c(x_bf16, np.uint16)
+    d = x.shape[-1]
+    n = x.size // d if d else 0
+    x_rt = np.empty_like(x)
+    codes = np.empty(x.shape, np.uint8)
+    scales = np.empty(x.shape[:-1] + (d // 32,), np.uint8)
+    rc = lib.or_act_quant(_ptr(x), n, d, _ptr(x_rt), _ptr(codes), _ptr(scales))
+    if rc != OK:
+        raise ValueError(f"or_act_quant failed ({rc})")
+    return x_rt, codes, scales
+
+
+def window_idxs(start_pos: int, seqlen: int, window: int) -> np.ndarray:
+    """[seqlen][window] int32 slot indices (prefill: start_pos == 0; decode: seqlen == 1)."""
+    lib = _load()
+    out = np.empty((seqlen, window), np.int32)
+    rc = lib.or_window_idxs(start_pos, seqlen, window, _ptr(out), window)
+    if rc == UNSUPPORTED:
+        raise NotImplementedError("chunked prefill (start_pos > 0 and seqlen > 1)")
+    if rc != OK:
+        raise ValueError(f"or_window_idxs failed ({rc})")
+    return out
+
+
+def ring_write(ring: np.ndarray, rows: np.ndarray, start_pos: int) -> None:
+    """Write kv rows [seqlen][d] (bf16 bits) for positions start_pos.. into ring [window][d]."""
+    lib = _load()
+    assert ring.dtype == np.uint16 and ring.flags.c_contiguous
+    r = _c(rows, np.uint16)
+    rc = lib.or_ring_write(_ptr(ring), _ptr(r), start_pos, r.shape[0], ring.shape[0], ring.shape[1])
+    if rc != OK:
+        raise ValueError(f"or_ring_write failed ({rc})")
+
+
+def sparse_attn(q, kv, sink, idx, scale, *, kv_scales=None, tokens=None, nthreads=None,
+                want_f64=False):
+    """The plain definition of sparse_attn.
+
+    q      uint16 [b, s, h, d] bf16 bits
+    kv     uint16 [b, rows, d] bf16 bits, or (kv_scales given) uint8 e4m3 codes [b, rows, d]
+    kv_scales uint8 [b, rows, d/32] e8m0, or None
+    sink   float32 [h]
+    idx    int32 [b, s, topk], -1 = empty
+    scale  softmax scale, used as the f32 value
+    tokens optional int64 list of flat token ids (b_i * s + s_i): only those are computed and the
+           result is [len(tokens), h, d]; otherwise [b, s, h, d].
+    Returns bf16 bits (uint16) and, with want_f64, the unrounded f64 result as a second value.
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    b, s, h, d = q.shape
+    fmt = 0 if kv_scales is None else 1
+    kv = _c(kv, np.uint16 if fmt == 0 else np.uint8)
+    rows = kv.shape[1]
+    sc = None if kv_scales is None else _c(kv_scales, np.uint8)
+    sink = _c(sink, np.float32)
+    idx = _c(idx, np.int32)
+    topk = idx.shape[-1]
+    assert idx.shape == (b, s, topk) and kv.shape == (b, rows, d) and sink.shape == (h,)
+    if tokens is None:
+        tk = None
+        out_shape = (b, s, h, d)
+        nt = b * s
+    else:
+        tk = _c(tokens, np.int64)
+        nt = tk.size
+        out_shape = (nt, h, d)
+    o = np.empty(out_shape, np.uint16)
+    o64 = np.empty(out_shape, np.float64) if want_f64 else None
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = lib.or_sparse_attn(_ptr(q), _ptr(kv) if fmt == 0 else None,
+                            _ptr(kv) if fmt == 1 else None, _ptr(sc), fmt, _ptr(sink), _ptr(idx),
+                            float(np.float32(scale)), b, s, h, d, rows, topk, _ptr(tk), nt,
+                            _ptr(o), _ptr(o64), int(nthreads))
+    if rc == BAD_INDEX:
+        raise IndexError("an index is outside [-1, rows)")
+    if rc != OK:
+        raise ValueError(f"or_sparse_attn failed ({rc})")
+    return (o, o64) if want_f64 else o

@@ -1,0 +1,399 @@
+"""Pins of the CPU oracle to facts outside itself: library routines, closed forms, invariants,
+brute force and the pages' worked examples.  No GPU needed."""
+
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from sparse_latent_attention_gb300 import workloads
+from tests._helpers import bf16_to_f64, compose_idx_oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------------------------
+# small random problems
+# --------------------------------------------------------------------------------------------
+
+def _problem(seed, b=2, s=3, h=5, d=32, rows=20, topk=9, neg=0.2, distinct=True):
+    rng = np.random.default_rng(seed)
+    q = workloads.to_bf16_bits(rng.standard_normal((b, s, h, d), dtype=np.float32))
+    kv = workloads.to_bf16_bits(rng.standard_normal((b, rows, d), dtype=np.float32))
+    sink = rng.standard_normal(h).astype(np.float32)
+    if distinct:
+        idx = np.stack([np.stack([rng.choice(rows, topk, replace=False) for _ in range(s)])
+                        for _ in range(b)]).astype(np.int32)
+    else:
+        idx = rng.integers(0, rows, (b, s, topk)).astype(np.int32)
+    idx[rng.random(idx.shape) < neg] = -1
+    scale = np.float32(d ** -0.5)
+    return q, kv, sink, idx, scale
+
+
+def _dense_reference(q, kv, sink, idx, scale):
+    """Brute force: a dense [h, rows] logit matrix per token, every unlisted row masked to -inf,
+    listed rows weighted by their multiplicity (log count added), one extra sink column whose
+    value row is zero, and scipy's softmax over the lot."""
+    b, s, h, d = q.shape
+    rows = kv.shape[1]
+    qf, kf = bf16_to_f64(q), bf16_to_f64(kv)
+    out = np.zeros((b, s, h, d))
+    for bi in range(b):
+        for si in range(s):
+            counts = np.bincount(idx[bi, si][idx[bi, si] >= 0], minlength=rows).astype(float)
+            if counts.sum() == 0:
+                continue
+            logits = float(np.float32(scale)) * (qf[bi, si] @ kf[bi].T)  # [h, rows]
+            with np.errstate(divide="ignore"):
+                logits = logits + np.log(counts)[None, :]  # -inf where unlisted
+            full = np.concatenate([logits, sink.astype(np.float64)[:, None]], axis=1)
+            p = scipy.special.softmax(full, axis=1)
+            values = np.concatenate([kf[bi], np.zeros((1, d))], axis=0)
+            out[bi, si] = p @ values
+    return out
+
+
+@pytest.mark.parametrize("seed,distinct", [(11, True), (12, True), (13, False)])
+def test_sparse_attn_matches_dense_masked_softmax(seed, distinct):
+    q, kv, sink, idx, scale = _problem(seed, distinct=distinct)
+    idx[0, 1, :] = -1  # one token with nothing listed
+    o, o64 = oracle.sparse_attn(q, kv, sink, idx, scale, want_f64=True)
+    ref = _dense_reference(q, kv, sink, idx, scale)
+    np.testing.assert_allclose(o64, ref, rtol=1e-12, atol=1e-13)
+    # the bf16 output is the rounding of the f64 result, checked against torch's f64 -> bf16
+    # conversion where f32 holds the value exactly
+    t = torch.from_numpy(o64.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    agree = (t.view(np.uint16) == o).mean()
+    assert agree > 0.999
+
+
+def test_sink_to_minus_inf_is_plain_softmax():
+    q, kv, sink, idx, scale = _problem(21, neg=0.0)
+    ninf = np.full_like(sink, -np.inf)
+    _, o64 = oracle.sparse_attn(q, kv, ninf, idx, scale, want_f64=True)
+    qf, kf = bf16_to_f64(q), bf16_to_f64(kv)
+    for bi in range(q.shape[0]):
+        for si in range(q.shape[1]):
+            g = kf[bi, idx[bi, si]]
+            p = scipy.special.softmax(float(scale) * qf[bi, si] @ g.T, axis=1)
+            np.testing.assert_allclose(o64[bi, si], p @ g, rtol=1e-12, atol=1e-13)
+    # a very negative finite sink approaches the same limit
+    _, o64b = oracle.sparse_attn(q, kv, np.full_like(sink, -1e4), idx, scale, want_f64=True)
+    np.testing.assert_allclose(o64b, o64, rtol=1e-12, atol=1e-13)
+
+
+def test_index_order_invariance():
+    q, kv, sink, idx, scale = _problem(31, topk=15)
+    o, o64 = oracle.sparse_attn(q, kv, sink, idx, scale, want_f64=True)
+    rng = np.random.default_rng(5)
+    perm = np.stack([np.stack([rng.permutation(idx.shape[-1]) for _ in range(idx.shape[1])])
+                     for _ in range(idx.shape[0])])
+    idx_p = np.take_along_axis(idx, perm, axis=-1)
+    o2, o64b = oracle.sparse_attn(q, kv, sink, idx_p, scale, want_f64=True)
+    np.testing.assert_allclose(o64b, o64, rtol=1e-12, atol=1e-14)
+    same = (o2 == o).mean()
+    assert same >= 0.999
+    diff = np.abs(o2.astype(np.int32) - o.astype(np.int32))
+    assert diff.max() <= 1
+
+
+def test_all_minus_one_row_is_exact_zero():
+    q, kv, sink, idx, scale = _problem(41)
+    idx[:] = -1
+    o = oracle.sparse_attn(q, kv, sink, idx, scale)
+    assert (o == 0).all()
+    # also with a sink of -inf (defined as 0)
+    o = oracle.sparse_attn(q, kv, np.full_like(sink, -np.inf), idx, scale)
+    assert (o == 0).all()
+
+
+def test_single_row_without_sink_returns_that_row_bit_exact():
+    q, kv, sink, idx, scale = _problem(51)
+    idx[:] = -1
+    idx[..., 3] = 7
+    o = oracle.sparse_attn(q, kv, np.full_like(sink, -np.inf), idx, scale)
+    for bi in range(q.shape[0]):
+        for si in range(q.shape[1]):
+            for hh in range(q.shape[2]):
+                assert (o[bi, si, hh] == kv[bi, 7]).all()
+
+
+def test_identical_rows_closed_form():
+    """All listed rows equal v: o = v * n / (n + exp(sink - l)), l = scale <q, v>."""
+    q, kv, sink, idx, scale = _problem(61, neg=0.0)
+    kv[:] = kv[:, :1, :]  # every row is row 0
+    _, o64 = oracle.sparse_attn(q, kv, sink, idx, scale, want_f64=True)
+    qf, kf = bf16_to_f64(q), bf16_to_f64(kv)
+    n = idx.shape[-1]
+    for bi in range(q.shape[0]):
+        v = kf[bi, 0]
+        l = float(scale) * (qf[bi] @ v)  # [s, h]
+        w = n / (n + np.exp(sink.astype(np.float64)[None, :] - l))
+        np.testing.assert_allclose(o64[bi], w[..., None] * v[None, None, :], rtol=1e-12,
+                                   atol=1e-14)
+
+
+def test_output_bounded_by_gathered_rows():
+    q, kv, sink, idx, scale = _problem(71, topk=12)
+    _, o64 = oracle.sparse_attn(q, kv, sink, idx, scale, want_f64=True)
+    kf = bf16_to_f64(kv)
+    for bi in range(q.shape[0]):
+        for si in range(q.shape[1]):
+            live = idx[bi, si][idx[bi, si] >= 0]
+            bound = np.abs(kf[bi, live]).max(axis=0) if live.size else np.zeros(q.shape[-1])
+            assert (np.abs(o64[bi, si]) <= bound[None, :] * (1 + 1e-15)).all()
+
+
+def test_fp8_storage_equals_round_trip():
+    """Attention over e4m3 codes + e8m0 scales equals attention over their bf16 round trip."""
+    q, kv, sink, idx, scale = _problem(81, d=64)
+    rt, codes, scales = oracle.act_quant(kv)
+    a = oracle.sparse_attn(q, rt, sink, idx, scale)
+    bq = oracle.sparse_attn(q, codes, sink, idx, scale, kv_scales=scales)
+    assert (a == bq).all()
+
+
+def test_out_of_range_index_refused():
+    q, kv, sink, idx, scale = _problem(91)
+    idx[0, 0, 0] = kv.shape[1]
+    with pytest.raises(IndexError):
+        oracle.sparse_attn(q, kv, sink, idx, scale)
+    idx[0, 0, 0] = -2
+    with pytest.raises(IndexError):
+        oracle.sparse_attn(q, kv, sink, idx, scale)
+
+
+def test_token_subset_matches_full():
+    q, kv, sink, idx, scale = _problem(101, b=3, s=4)
+    full = oracle.sparse_attn(q, kv, sink, idx, scale)
+    toks = np.array([0, 5, 11, 7])
+    part = oracle.sparse_attn(q, kv, sink, idx, scale, tokens=toks)
+    assert (part == full.reshape(-1, *full.shape[2:])[toks]).all()
+
+
+def test_tiny_workload_against_dense():
+    wl = workloads.make_named("tiny")
+    idx = compose_idx_oracle(wl)
+    assert (idx[0, 11] == -1).all()
+    kv = wl.kv_raw_dense()
+    _, o64 = oracle.sparse_attn(wl.q, kv, wl.sink, idx, wl.scale, want_f64=True)
+    np.testing.assert_allclose(o64, _dense_reference(wl.q, kv, wl.sink, idx, wl.scale),
+                               rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------------------------
+# bf16 rounding
+# --------------------------------------------------------------------------------------------
+
+def test_bf16_round_matches_torch_on_f32_values():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(200000).astype(np.float32),
+                        (rng.standard_normal(50000) * 1e-39).astype(np.float32),  # subnormal
+                        (rng.standard_normal(50000) * 1e37).astype(np.float32),
+                        np.array([0.0, -0.0, 3.3895314e38, -3.3895314e38], np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_round(x.astype(np.float64))
+    assert (got == want).all()
+
+
+def test_bf16_round_f64_brute_force_nearest():
+    """For f64 inputs (finer than f32) the result is the nearest bf16, ties to even mantissa."""
+    rng = np.random.default_rng(4)
+    # bf16 neighbours and their exact midpoints, nudged by tiny f64 amounts
+    base = workloads.to_bf16_bits(rng.standard_normal(20000).astype(np.float32))
+    lo = bf16_to_f64(base)
+    hi = bf16_to_f64((base.astype(np.int32) + 1).astype(np.uint16))  # next magnitude
+    mid = (lo + hi) / 2
+    for x in (mid, mid + np.abs(mid) * 1e-12, mid - np.abs(mid) * 1e-12, lo + (hi - lo) * 0.3):
+        got = bf16_to_f64(oracle.bf16_round(x))
+        dlo, dhi = np.abs(x - lo), np.abs(x - hi)
+        want = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi,
+                        np.where(base % 2 == 0, lo, hi)))
+        assert (got == want).all()
+
+
+# --------------------------------------------------------------------------------------------
+# e4m3 codec
+# --------------------------------------------------------------------------------------------
+
+def test_e4m3_decode_all_codes_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_decode(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert set(np.nonzero(nan)[0]) == {0x7F, 0xFF}
+    assert np.isnan(got[nan]).all()
+    assert (got[~nan] == want[~nan]).all()
+    assert got[~nan].max() == 448.0 and got[~nan].min() == -448.0
+
+
+def _e4m3_finite_values():
+    v = oracle.e4m3_decode(np.arange(128, dtype=np.uint8))
+    return np.arange(128)[~np.isnan(v)], v[~np.isnan(v)]
+
+
+def test_e4m3_encode_matches_torch_and_brute_force():
+    rng = np.random.default_rng(6)
+    codes, vals = _e4m3_finite_values()
+    mids = (vals[1:] + vals[:-1]) / 2
+    x = np.concatenate([
+        rng.standard_normal(300000) * 30, rng.standard_normal(100000) * 0.01,
+        rng.uniform(-460, 460, 100000), vals, -vals, mids, -mids,
+        np.nextafter(mids, 0), np.nextafter(mids, 1000)]).astype(np.float32)
+    x = x[np.abs(x) < 464]  # torch turns larger magnitudes into NaN rather than saturating
+    got = oracle.e4m3_encode(x)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (got == want).all()
+    # brute force on the mids and a sample: nearest finite value, ties to the even code
+    xs = np.concatenate([mids, x[:20000].astype(np.float64)])
+    a = np.abs(xs)
+    dist = np.abs(a[:, None] - vals[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    pick_even = cand & (codes[None, :] % 2 == 0)
+    choose = np.where(cand.sum(1) > 1, pick_even.argmax(1), cand.argmax(1))
+    want_code = codes[choose] | np.where(np.signbit(xs), 0x80, 0)
+    want_code = np.where(a == 0, np.where(np.signbit(xs), 0x80, 0), want_code)
+    assert (oracle.e4m3_encode(xs.astype(np.float32)) == want_code).all()
+
+
+def test_e4m3_encode_saturates():
+    x = np.array([464, 480, 1e6, 3e38, -500, -1e9], np.float32)
+    assert (oracle.e4m3_encode(x) == np.array([0x7E] * 4 + [0xFE] * 2, np.uint8)).all()
+
+
+# --------------------------------------------------------------------------------------------
+# pow2_ceil
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.slow
+def test_pow2_ceil_exhaustive():
+    """Every positive normal f32 against 2 ** ceil(log2 v) from numpy's frexp."""
+    lo, hi = 0x00800000, 0x7F7FFFFF
+    step = 1 << 24
+    for start in range(lo, hi + 1, step):
+        bits = np.arange(start, min(start + step, hi + 1), dtype=np.uint32)
+        v = bits.view(np.float32)
+        m, e = np.frexp(v)  # v = m * 2^e, 0.5 <= m < 1
+        ce = np.where(m == 0.5, e - 1, e)
+        with np.errstate(over="ignore"):
+            want = np.ldexp(np.float32(1.0), ce).astype(np.float32)
+        got = oracle.pow2_ceil(v)
+        assert (got.view(np.uint32) == want.view(np.uint32)).all(), hex(start)
+
+
+# --------------------------------------------------------------------------------------------
+# act_quant
+# --------------------------------------------------------------------------------------------
+
+def _read_act_quant_examples():
+    out = []
+    for line in open(os.path.join(GOLDEN, "act_quant_examples.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        head, tail = line.split("|")
+        parts = head.split()
+        out.append((parts[0], int(parts[1]), [float(t) for t in parts[2:]],
+                    [float(t) for t in tail.split()]))
+    return out
+
+
+@pytest.mark.parametrize("case", _read_act_quant_examples(), ids=lambda c: c[0])
+def test_act_quant_worked_examples(case):
+    name, e8m0, xin, xout = case
+    x = np.zeros(32, np.float32)
+    x[: len(xin)] = xin
+    bits = workloads.to_bf16_bits(x)
+    assert (bf16_to_f64(bits)[: len(xin)] == np.array(xin)).all(), "inputs must be bf16 values"
+    rt, codes, scales = oracle.act_quant(bits[None])
+    assert scales[0, 0] == e8m0
+    got = bf16_to_f64(rt[0])
+    assert (got[: len(xout)] == np.array(xout)).all(), got[: len(xout)]
+    assert (got[len(xout):] == 0).all()
+
+
+def test_act_quant_properties():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((64, 512)).astype(np.float32)
+    x *= np.exp(rng.uniform(-20, 20, (64, 16))).repeat(32, axis=1).astype(np.float32)
+    bits = workloads.to_bf16_bits(x)
+    rt, codes, scales = oracle.act_quant(bits)
+    xf = bf16_to_f64(bits).reshape(64, 16, 32)
+    rtf = bf16_to_f64(rt).reshape(64, 16, 32)
+    s = np.ldexp(1.0, scales.astype(np.int32) - 127)[..., None]
+    amax = np.maximum(np.abs(xf).max(-1, keepdims=True), float(np.float32(1e-4)))
+    # the scale is the smallest power of two that brings amax / s to <= 448
+    assert (amax / s <= 448).all() and ((amax / (s / 2) > 448) | (s <= 2.0 ** -22)).all()
+    # dequantised values are codes times scale, and the codes decode to the round trip
+    dec = oracle.e4m3_decode(codes).reshape(64, 16, 32)
+    assert (dec * s == rtf).all()
+    # round to nearest: error at most half an e4m3 step of the value's binade (or subnormal step)
+    y = xf / s
+    step = np.where(np.abs(y) < 2.0 ** -6, 2.0 ** -9,
+                    np.ldexp(1.0, np.floor(np.log2(np.maximum(np.abs(y), 1e-300))).astype(int) - 3))
+    assert (np.abs(dec - y) <= step / 2 + 0.0).all()
+    # the round trip is idempotent (codes and scales need not be: a block whose amax rounded
+    # down onto 448 * 2^k takes the smaller scale the second time, with the same values)
+    rt2, codes2, scales2 = oracle.act_quant(rt)
+    assert (rt2 == rt).all()
+    s2 = np.ldexp(1.0, scales2.astype(np.int32) - 127)[..., None]
+    assert (oracle.e4m3_decode(codes2).reshape(64, 16, 32) * s2 == rtf).all()
+
+
+# --------------------------------------------------------------------------------------------
+# window indices and the ring cache
+# --------------------------------------------------------------------------------------------
+
+def _golden_ring():
+    g = {}
+    for line in open(os.path.join(GOLDEN, "ring_example.txt")):
+        line = line.split("#")[0].strip()
+        if line:
+            k, _kind, *vals = line.split()
+            g[k] = [int(v) for v in vals]
+    return g
+
+
+def test_ring_worked_example():
+    g = _golden_ring()
+    W = g["window"][0]
+    n = g["prefill_tokens"][0]
+    ring = np.full((W, 1), 0xFFFF, np.uint16)
+    tokens = np.arange(n + 2, dtype=np.uint16)[:, None]  # a row's value is its token number
+    oracle.ring_write(ring, tokens[:n], 0)
+    assert ring[:, 0].tolist() == g["prefill_ring"]
+    for p in (12, 13):
+        oracle.ring_write(ring, tokens[p:p + 1], p)
+        assert int(np.nonzero(ring[:, 0] == p)[0][0]) == g[f"decode{p}_slot"][0]
+        assert ring[:, 0].tolist() == g[f"decode{p}_ring"]
+        idx = oracle.window_idxs(p, 1, W)[0]
+        assert idx.tolist() == g[f"decode{p}_idx"]
+        # the ring read in column order is the last W tokens, oldest first
+        assert ring[idx, 0].tolist() == list(range(p - W + 1, p + 1))
+    assert oracle.window_idxs(0, n, W)[3].tolist() == g["prefill_row3"]
+
+
+def test_window_idxs_cases():
+    # prefill: causal window, row i covers positions i-W+1..i
+    w = oracle.window_idxs(0, 300, 128)
+    for i in (0, 1, 127, 128, 299):
+        row = w[i]
+        want = [p if p >= 0 else -1 for p in range(i - 127, i + 1)]
+        assert row.tolist() == want
+    # shorter chunk than the window: still W columns, -1 first
+    assert oracle.window_idxs(0, 3, 8).tolist()[2] == [-1] * 5 + [0, 1, 2]
+    # decode before the ring is full: -1 first, then slots of positions 0..p
+    assert oracle.window_idxs(5, 1, 8).tolist() == [[-1, -1, 0, 1, 2, 3, 4, 5]]
+    # decode with a full ring at a multiple of W: oldest slot is (p+1) mod W
+    assert oracle.window_idxs(32768, 1, 128)[0].tolist() == list(range(1, 128)) + [0]
+    with pytest.raises(NotImplementedError):
+        oracle.window_idxs(4, 3, 8)
+    # empty chunk
+    assert oracle.window_idxs(0, 0, 8).shape == (0, 8)
