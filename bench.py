@@ -1,0 +1,567 @@
+#!/usr/bin/env python
+"""Throughput of the sparse_attn hot path on GB300, as one JSON line.
+
+A step is one pass of the whole path over one batch of synthetic input:
+  1. window_idxs   -- the window columns of idx (the compressed columns are resident input)
+  2. act_quant     -- the kv rows this step produces: the chunk's rows (prefill) or one new
+                      row per sequence written into its ring slot (decode)
+  3. sparse_attn   -- the index-gathered attention with the sink
+The metric is query-heads per second (b * s * h per step time).  `value` is device time with
+inputs resident in HBM (L2 flushed between steps, each step timed with CUDA events on the
+launching stream); `e2e` times the same step through the public API with the step's inputs
+copied from pinned host memory and the output read back.  `roofline` relates the sparse_attn
+launch to the binding roofline (HBM bytes or dense bf16 FLOPs), and `cpu_baseline` times the CPU
+oracle on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+N > 1 is launched by torchrun, one rank per GPU; every rank runs its own copy of the workload
+(the path has no exchange step: weak scaling) and the slowest rank's time counts.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_latent_attention_gb300 import workloads  # noqa: E402
+
+METRIC = ("sparse_attn query·heads/s and % of roofline (HBM GB/s decode, tensor-pipe "
+          "prefill)")
+UNIT = "query·heads/s"
+DEFAULT_WORKLOAD = "swa_prefill"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+
+# dram__bytes_read.sum + dram__bytes_write.sum per sparse_attn launch, from the committed ncu
+# captures under profiles/, keyed by (library version, workload).  Absent -> null.
+NCU_TRAFFIC = {}
+
+
+# --------------------------------------------------------------------------------------------
+# multi-rank plumbing (host side; covered by the gloo tests)
+# --------------------------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (x itself at world size 1)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: every rank processed units_per_rank in at most seconds_max."""
+    return units_per_rank * world / seconds_max
+
+
+# --------------------------------------------------------------------------------------------
+# measured peaks, clocks
+# --------------------------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the benchmark runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return self
+        threading.Thread(target=self._read, daemon=True).start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if len(inside) < 3:  # a short timed region: widen to the run around it
+            inside = [p for t, p in self.samples]
+            window = "warm-up + timed run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        smax = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside), "window": window,
+                "power_w_max": max((num(p[2]) or 0.0) for p in inside)}
+
+
+def gpu_id_of(torch, dev) -> str | None:
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:  # noqa: BLE001
+        return None
+
+
+# --------------------------------------------------------------------------------------------
+# the workload's algorithmic bytes and FLOPs
+# --------------------------------------------------------------------------------------------
+
+def unique_kv_bytes(wl, idx_np: np.ndarray) -> int:
+    total = 0
+    for bi in range(wl.b):
+        u = np.unique(idx_np[bi])
+        total += int((u >= 0).sum())
+    return total * wl.kv_row_bytes()
+
+
+def roofline_terms(wl, idx_np, peaks):
+    q_bytes = wl.q_bytes()
+    o_bytes = q_bytes
+    kv_bytes = unique_kv_bytes(wl, idx_np)
+    alg_bytes = q_bytes + o_bytes + kv_bytes
+    flops = wl.flops()
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    return dict(alg_bytes=alg_bytes, kv_bytes=kv_bytes, flops=flops, t_hbm=t_hbm, t_tc=t_tc,
+                bound="hbm" if t_hbm >= t_tc else "tensor")
+
+
+# --------------------------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------------------------
+
+class GpuPath:
+    """Device buffers of one workload and its step through the library."""
+
+    def __init__(self, wl, dev):
+        import torch
+
+        import sparse_latent_attention_gb300 as sa
+        self.torch, self.sa, self.wl, self.dev = torch, sa, wl, dev
+        bf16 = torch.bfloat16
+
+        def to_dev_bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(bf16).to(dev)
+
+        self.fp8 = wl.kv_format == "fp8"
+        self.decode = wl.s == 1 and wl.start_pos > 0
+        self.q = to_dev_bf16(wl.q)
+        self.sink = torch.from_numpy(wl.sink).to(dev)
+        self.idx = torch.full((wl.b, wl.s, wl.topk), -1, dtype=torch.int32, device=dev)
+        self.idx[:, :, wl.window:] = torch.from_numpy(wl.idx_tail).to(dev)
+        # every kv row in raw form, quantised once here; the step re-quantises the rows it owns
+        raw = torch.zeros((wl.b, wl.rows, wl.d), dtype=bf16, device=dev)
+        rows = torch.from_numpy(wl.kv_rows).to(dev)
+        raw[torch.arange(wl.b, device=dev)[:, None].expand_as(rows), rows] = to_dev_bf16(wl.kv_vals)
+        d = wl.d
+        if self.fp8:
+            self.kv = torch.empty((wl.b, wl.rows, d), dtype=torch.uint8, device=dev)
+            self.kv_scale = torch.empty((wl.b, wl.rows, d // 32), dtype=torch.uint8, device=dev)
+            sa.act_quant_fp8(raw.view(-1, d), codes=self.kv.view(-1, d),
+                             scales=self.kv_scale.view(-1, d // 32))
+        else:
+            self.kv = raw.clone()
+            self.kv_scale = None
+            sa.act_quant_fp8(self.kv.view(-1, d), out_rt=self.kv.view(-1, d))
+        if self.decode:
+            self.slot = wl.start_pos % wl.window
+            self.new_rows = raw[:, self.slot, :].contiguous()   # this step's latent row per sequence
+        else:
+            self.new_rows = raw[:, : wl.s, :].contiguous()      # the chunk's latent rows
+        del raw
+        self.o = torch.empty_like(self.q)
+        self.ws = sa.new_workspace(wl.b, wl.s, wl.h, d, wl.rows, wl.topk,
+                                   sa.SA_KV_FP8_E4M3 if self.fp8 else sa.SA_KV_BF16, device=dev)
+        self.launches_per_step = 2 + (2 if self.ws.numel() > sa.SA_STATUS_BYTES else 1)
+
+    def step(self, ev=None):
+        """One pass of the path; ev = (start, end) CUDA events bracketing sparse_attn."""
+        sa, wl, d = self.sa, self.wl, self.wl.d
+        sa.window_idxs(wl.start_pos, wl.s, wl.window, out=self.idx[:, :, : wl.window], nbatch=wl.b)
+        if self.decode:
+            if self.fp8:
+                sa.act_quant_fp8(self.new_rows, codes=self.kv[:, self.slot, :],
+                                 scales=self.kv_scale[:, self.slot, :])
+            else:
+                sa.act_quant_fp8(self.new_rows, out_rt=self.kv[:, self.slot, :])
+        else:
+            nr = self.new_rows.view(-1, d)
+            sa.act_quant_fp8(nr, out_rt=self.kv[:, : wl.s, :].reshape(-1, d))
+        if ev is not None:
+            ev[0].record()
+        sa.sparse_attn(self.q, self.kv, self.sink, self.idx, wl.scale, kv_scale=self.kv_scale,
+                       out=self.o, workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rank0 = rank == 0
+    peaks = load_peaks()
+    wl = workloads.make_named(args.workload)
+    path = GpuPath(wl, dev)
+    path.step()
+    torch.cuda.synchronize()
+    idx_np = path.idx.cpu().numpy()
+    terms = roofline_terms(wl, idx_np, peaks)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    sampler = ClockSampler(gpu_id_of(torch, dev)).start() if rank0 else None
+    for _ in range(args.warmup):
+        flush.zero_()
+        path.step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, each bracketed by events; L2 flushed between steps (not timed)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for e in ev:
+        flush.zero_()
+        e[0].record()
+        path.step(ev=(e[2], e[3]))
+        e[1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
+    attn_ms = [c.elapsed_time(d) for _, _, c, d in ev]
+    assert path.sa.read_status(path.ws) == 0, "kernel reported an out-of-range index"
+
+    # end to end through the public API: host inputs in, host output out, every step
+    pin = dict(q=path.q.cpu().pin_memory(), rows=path.new_rows.cpu().pin_memory(),
+               sink=path.sink.cpu().pin_memory(),
+               idx=path.idx.cpu().pin_memory() if wl.topk > wl.window else None,
+               o=torch.empty(path.o.shape, dtype=path.o.dtype).pin_memory())
+    h2d = (pin["q"].numel() * 2 + pin["rows"].numel() * 2 + pin["sink"].numel() * 4 +
+           (pin["idx"].numel() * 4 if pin["idx"] is not None else 0))
+    d2h = pin["o"].numel() * 2
+
+    def e2e_step():
+        path.q.copy_(pin["q"], non_blocking=True)
+        path.new_rows.copy_(pin["rows"], non_blocking=True)
+        path.sink.copy_(pin["sink"], non_blocking=True)
+        if pin["idx"] is not None:
+            path.idx.copy_(pin["idx"], non_blocking=True)
+        path.step()
+        pin["o"].copy_(path.o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if sampler:
+        sampler.stop()
+
+    units = wl.n_tokens * wl.h
+    ms_step = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    ms_attn = max_over_ranks(sum(attn_ms) / len(attn_ms), world, dev)
+    ms_e2e = max_over_ranks(e2e_ms, world, dev)
+    if not rank0:
+        return None
+    value = job_value(units, world, ms_step / 1e3)
+    bound = terms["bound"]
+    t_attn = ms_attn / 1e3
+    gbs = terms["alg_bytes"] / t_attn / 1e9
+    tfs = terms["flops"] / t_attn / 1e12
+    lib_version = path.sa._lib.version()
+    traffic = NCU_TRAFFIC.get((lib_version, wl.name))
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic}
+        other = {"unit": "TFLOP/s", "achieved": round(tfs, 1), "peak": peaks["bf16_tflops"],
+                 "frac": round(tfs / peaks["bf16_tflops"], 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tfs, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(tfs / peaks["bf16_tflops"], 4),
+                "traffic": traffic}
+        other = {"unit": "GB/s", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                 "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    roof.update({"kernel": "sa_sparse_attn", "ms": round(ms_attn, 4),
+                 "alg_bytes": terms["alg_bytes"], "alg_flops": terms["flops"],
+                 "peak_source": peaks["source"] + " (burst)", "other": other,
+                 "roofline_ms": round(max(terms["t_hbm"], terms["t_tc"]) * 1e3, 4),
+                 "frac_of_roofline_time": round(max(terms["t_hbm"], terms["t_tc"]) / t_attn, 4)})
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3 kv, bf16 q/o, f32 accumulate" if path.fp8 else
+                 "bf16 (f32 accumulate)",
+        "data": "synthetic (seeded N(0,1) inputs with the workload's index structure)",
+        "config": {"workload": wl.name, "b": wl.b, "s": wl.s, "h": wl.h, "d": wl.d,
+                   "rows": wl.rows, "topk": wl.topk, "window": wl.window,
+                   "start_pos": wl.start_pos, "kv_format": wl.kv_format,
+                   "l2": "flushed between timed steps (256 MB write, outside the step events)",
+                   "parallelism": f"replica x{world}" if world > 1 else "1 GPU"},
+        "roofline": roof,
+        "e2e": {"value": round(job_value(units, world, ms_e2e / 1e3), 1), "unit": UNIT,
+                "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": path.launches_per_step * args.steps,
+        "clocks": sampler.summary(t0, t1) if sampler else None,
+        "lib_version": lib_version,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    return out
+
+
+# --------------------------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# --------------------------------------------------------------------------------------------
+
+class OracleStep:
+    """The path's step on the CPU oracle, on a sample of the workload's query tokens."""
+
+    def __init__(self, wl, seed=0):
+        import oracle
+        self.oracle, self.wl = oracle, wl
+        oracle.build()
+        self.threads = os.cpu_count() or 1
+        rng = np.random.default_rng(seed)
+        self.order = rng.permutation(wl.n_tokens)
+        self.pos = 0
+        # resident state prepared outside any timing: quantised cache rows and the idx tail
+        zrt, zc, zs = oracle.act_quant(np.zeros((1, wl.d), np.uint16))
+        self.zero_row = (zrt, zc, zs)
+        self.idx = np.full((wl.b, wl.s, wl.topk), -1, np.int32)
+        self.idx[:, :, wl.window:] = wl.idx_tail
+        self._cache = {}
+
+    def _seq_state(self, bi):
+        """Quantised kv of one sequence (rows that hold values quantised once, cached)."""
+        if bi not in self._cache:
+            wl, o = self.wl, self.oracle
+            rt_u, codes_u, sc_u = o.act_quant(wl.kv_vals[bi])
+            zrt, zc, zs = self.zero_row
+            if wl.kv_format == "fp8":
+                codes = np.broadcast_to(zc, (wl.rows, wl.d)).copy()
+                scales = np.broadcast_to(zs, (wl.rows, wl.d // 32)).copy()
+                codes[wl.kv_rows[bi]] = codes_u
+                scales[wl.kv_rows[bi]] = sc_u
+                self._cache[bi] = (codes, scales)
+            else:
+                rt = np.broadcast_to(zrt, (wl.rows, wl.d)).copy()
+                rt[wl.kv_rows[bi]] = rt_u
+                self._cache[bi] = (rt, None)
+        return self._cache[bi]
+
+    def prepare(self, tokens):
+        for bi in sorted(set((np.asarray(tokens) // self.wl.s).tolist())):
+            self._seq_state(bi)
+
+    def next_tokens(self, n):
+        if self.pos + n > len(self.order):
+            self.pos = 0
+        t = self.order[self.pos:self.pos + n]
+        self.pos += n
+        return np.sort(t)
+
+    def run(self, tokens):
+        """window_idxs + act_quant of the rows this step owns + attention for `tokens`."""
+        wl, o = self.wl, self.oracle
+        win = o.window_idxs(wl.start_pos, wl.s, wl.window)
+        self.idx[:, :, : wl.window] = win[None]
+        if wl.s == 1 and wl.start_pos > 0:
+            # one new row per sequence, in its ring slot (rows 0..window-1 lead kv_vals)
+            o.act_quant(wl.kv_vals[:, wl.start_pos % wl.window, :])
+        else:
+            o.act_quant(wl.kv_vals[0, : wl.s])  # the chunk's rows
+        by_seq = {}
+        for t in tokens:
+            by_seq.setdefault(int(t) // wl.s, []).append(int(t) % wl.s)
+        for bi, sl in by_seq.items():
+            kv, sc = self._seq_state(bi)
+            o.sparse_attn(wl.q[bi:bi + 1], kv[None], wl.sink, self.idx[bi:bi + 1], wl.scale,
+                          kv_scales=None if sc is None else sc[None], tokens=np.array(sl),
+                          nthreads=self.threads)
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    step = OracleStep(wl)
+    probe = step.next_tokens(min(8, wl.n_tokens))
+    step.prepare(probe)
+    t = time.perf_counter()
+    step.run(probe)
+    per_tok = (time.perf_counter() - t) / len(probe)
+    n = int(max(8, min(wl.n_tokens, budget_s / max(per_tok, 1e-9))))
+    tokens = step.next_tokens(n)
+    step.prepare(tokens)
+    t = time.perf_counter()
+    step.run(tokens)
+    dt = time.perf_counter() - t
+    return {"value": round(len(tokens) * wl.h / dt, 1), "unit": UNIT, "cores": step.threads,
+            "kind": "oracle",
+            "sample": f"{len(tokens)} of {wl.n_tokens} query tokens (all {wl.h} heads) of "
+                      f"{wl.name}, plus the step's window_idxs and act_quant; {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    wl = workloads.make_named(args.workload)
+    step = OracleStep(wl)
+    probe = step.next_tokens(min(8, wl.n_tokens))
+    step.prepare(probe)
+    t = time.perf_counter()
+    step.run(probe)
+    per_tok = (time.perf_counter() - t) / len(probe)
+    per_step_budget = args.ref_budget / max(1, args.steps + args.warmup)
+    n = int(max(1, min(wl.n_tokens, per_step_budget / max(per_tok, 1e-9))))
+    for _ in range(args.warmup):
+        tk = step.next_tokens(n)
+        step.prepare(tk)
+        step.run(tk)
+    times = []
+    for _ in range(args.steps):
+        tk = step.next_tokens(n)
+        step.prepare(tk)  # cache preparation is setup, outside the timed step
+        t = time.perf_counter()
+        step.run(tk)
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = n * wl.h * args.steps / total
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
+        "data": "synthetic (seeded N(0,1) inputs with the workload's index structure)",
+        "config": {"workload": wl.name, "b": wl.b, "s": wl.s, "h": wl.h, "d": wl.d,
+                   "rows": wl.rows, "topk": wl.topk, "tokens_per_step": n},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "kind": "oracle",
+                         "cores": step.threads,
+                         "sample": f"{n} query tokens per step (all heads) of {wl.name}"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[n for n in workloads.NAMED])
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--ref-budget", type=float, default=90.0,
+                    help="seconds of oracle work for the whole --impl reference run")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            ap.error("--gpus N > 1 is launched with torchrun (one rank per GPU)")
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        dist_init("nccl")
+        out = run_gpu(args, rank, world, local)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

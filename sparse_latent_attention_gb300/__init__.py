@@ -1,0 +1,152 @@
+"""sparse_attn for GB300: DeepSeek V4.1's index-gathered latent attention with an attention sink.
+
+The public calls take torch CUDA tensors and pass their device pointers to the C-ABI library
+(libsa.so, include/sparse_attn.h) on the current stream.  PyTorch provides device memory and
+streams only; all the arithmetic runs in the library's sm_103a kernels.
+
+    o = sparse_attn(q, kv, sink, idx, softmax_scale)            # bf16 kv
+    o = sparse_attn(q, codes, sink, idx, scale, kv_scale=e8m0)  # fp8 e4m3 kv + e8m0 scales
+    window_idxs(start_pos, seqlen, window, out=idx[..., :window])
+    act_quant_fp8(x, out_rt=x)                                  # in-place block-32 round trip
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (SA_KV_BF16, SA_KV_FP8_E4M3, SA_STATUS_BYTES, SparseAttnError, load,
+                   status_string)
+
+__all__ = ["sparse_attn", "window_idxs", "act_quant_fp8", "workspace_size", "new_workspace",
+           "read_status", "SparseAttnError", "SA_KV_BF16", "SA_KV_FP8_E4M3", "load"]
+
+
+def _ptr(t) -> ctypes.c_void_p | None:
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, device=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def workspace_size(b, s, h, d, rows, topk, kv_format=SA_KV_BF16) -> int:
+    n = int(load().sa_sparse_attn_workspace_size(b, s, h, d, rows, topk, kv_format))
+    if n == 0:
+        raise SparseAttnError(_lib.SA_ERR_UNSUPPORTED, "sa_sparse_attn_workspace_size")
+    return n
+
+
+def new_workspace(b, s, h, d, rows, topk, kv_format=SA_KV_BF16, device="cuda") -> torch.Tensor:
+    """A zeroed uint8 workspace of the size the library asks for (status word cleared)."""
+    return torch.zeros(workspace_size(b, s, h, d, rows, topk, kv_format), dtype=torch.uint8,
+                       device=device)
+
+
+def sparse_attn(q, kv, sink, idx, softmax_scale, *, kv_scale=None, out=None, workspace=None,
+                stream=None) -> torch.Tensor:
+    """o[b, s, h, d] (bf16) = sparse_attn(q, kv, sink, idx, softmax_scale).
+
+    q [b, s, h, d] bf16; kv [b, rows, d] bf16, or uint8 e4m3 codes with kv_scale [b, rows, d/32]
+    uint8 e8m0; sink [h] f32; idx [b, s, topk] int32 (-1 = empty)."""
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    b, s, h, d = q.shape
+    fmt = SA_KV_BF16 if kv_scale is None else SA_KV_FP8_E4M3
+    _need(kv, "kv", torch.bfloat16 if fmt == SA_KV_BF16 else torch.uint8, dev)
+    if kv.dim() != 3 or kv.shape[0] != b or kv.shape[2] != d:
+        raise ValueError(f"kv shape {tuple(kv.shape)} does not match q {tuple(q.shape)}")
+    rows = kv.shape[1]
+    if kv_scale is not None:
+        _need(kv_scale, "kv_scale", torch.uint8, dev)
+        if tuple(kv_scale.shape) != (b, rows, d // 32):
+            raise ValueError(f"kv_scale shape {tuple(kv_scale.shape)} != {(b, rows, d // 32)}")
+    _need(sink, "sink", torch.float32, dev)
+    if tuple(sink.shape) != (h,):
+        raise ValueError(f"sink shape {tuple(sink.shape)} != ({h},)")
+    _need(idx, "idx", torch.int32, dev)
+    if idx.dim() != 3 or idx.shape[0] != b or idx.shape[1] != s:
+        raise ValueError(f"idx shape {tuple(idx.shape)} does not match q {tuple(q.shape)}")
+    topk = idx.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = new_workspace(b, s, h, d, rows, topk, fmt, device=dev)
+    else:
+        _need(workspace, "workspace", torch.uint8, dev)
+    st = load().sa_sparse_attn(_ptr(q), _ptr(kv), _ptr(kv_scale), fmt, _ptr(sink), _ptr(idx),
+                               float(softmax_scale), b, s, h, d, rows, topk, _ptr(out),
+                               _ptr(workspace), workspace.numel(), _stream(stream))
+    _lib.check(st, "sa_sparse_attn")
+    return out
+
+
+def window_idxs(start_pos, seqlen, window, *, out=None, nbatch=1, stream=None, device="cuda"):
+    """Window index table [nbatch, seqlen, window] (int32), written into ``out`` when given
+    (``out`` may be a column slice of a wider idx tensor: its row and batch strides are used)."""
+    if out is None:
+        out = torch.empty((nbatch, seqlen, window), dtype=torch.int32, device=device)
+    if out.dtype != torch.int32 or not out.is_cuda:
+        raise TypeError("out must be a CUDA int32 tensor")
+    if out.dim() == 2:
+        out3 = out.unsqueeze(0)
+    else:
+        out3 = out
+    if tuple(out3.shape) != (nbatch, seqlen, window) or out3.stride(2) != 1:
+        raise ValueError(f"out shape {tuple(out.shape)} / strides do not fit ({nbatch}, {seqlen}, "
+                         f"{window}) with unit column stride")
+    ld = out3.stride(1) if seqlen > 1 else max(window, out3.stride(1))
+    bstride = out3.stride(0) if nbatch > 1 else seqlen * ld
+    st = load().sa_window_idxs(start_pos, seqlen, window, _ptr(out3), ld, nbatch, bstride,
+                               _stream(stream))
+    _lib.check(st, "sa_window_idxs")
+    return out
+
+
+def act_quant_fp8(x, *, out_rt=None, codes=None, scales=None, stream=None):
+    """Block-32 e4m3 quantisation of the rows of a 2-D bf16 tensor (last dim contiguous).
+
+    Writes the bf16 round trip into ``out_rt`` (may be ``x`` itself), the e4m3 codes into
+    ``codes`` and the e8m0 block scales into ``scales`` (each a 2-D tensor with unit column
+    stride; rows may be strided, e.g. one ring slot per sequence of a cache)."""
+    if x.dim() != 2 or x.stride(1) != 1 or x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise ValueError("x must be a 2-D CUDA bf16 tensor with unit column stride")
+    n, d = x.shape
+
+    def rows_of(t, name, dtype, width):
+        if t is None:
+            return None, 0
+        if t.dim() != 2 or t.dtype != dtype or t.stride(1) != 1 or tuple(t.shape) != (n, width):
+            raise ValueError(f"{name} must be a 2-D {dtype} tensor of shape ({n}, {width}) with "
+                             "unit column stride")
+        return t, t.stride(0)
+
+    rt, rts = rows_of(out_rt, "out_rt", torch.bfloat16, d)
+    cd, cds = rows_of(codes, "codes", torch.uint8, d)
+    sc, scs = rows_of(scales, "scales", torch.uint8, d // 32)
+    st = load().sa_act_quant_fp8(_ptr(x), n, d, x.stride(0), _ptr(rt), rts, _ptr(cd), cds,
+                                 _ptr(sc), scs, _stream(stream))
+    _lib.check(st, "sa_act_quant_fp8")
+
+
+def read_status(workspace, clear=False, stream=None) -> int:
+    """The workspace status word as an sa_status (synchronises the stream)."""
+    return int(load().sa_read_status(_ptr(workspace), int(bool(clear)), _stream(stream)))

@@ -1,0 +1,153 @@
+// The C ABI declared in include/sparse_attn.h: argument checks, workspace layout and dispatch.
+// Nothing here allocates device memory; every kernel is enqueued on the caller's stream.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sa_internal.cuh"
+#include "sparse_attn.h"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+bool supported_shape(int64_t b, int64_t s, int h, int d, int64_t rows, int topk) {
+    if (b < 0 || s < 0 || rows < 0 || topk < 0) return false;
+    if (h < 1 || h > 128) return false;
+    if (d < 64 || d > 512 || d % 64 != 0) return false;
+    if (b * s * (int64_t)h >= (int64_t(1) << 31)) return false;
+    if (rows >= (int64_t(1) << 31)) return false;
+    return true;
+}
+
+sa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SA_OK : SA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t sa_sparse_attn_workspace_size(int64_t b, int64_t s, int h, int d, int64_t rows, int topk,
+                                     int kv_format) {
+    if (kv_format != SA_KV_BF16 && kv_format != SA_KV_FP8_E4M3) return 0;
+    if (!supported_shape(b, s, h, d, rows, topk)) return 0;
+    return SA_STATUS_BYTES + sa::align_up(sa::attn_mma_scratch_bytes(b, s, h, d, topk), 256);
+}
+
+sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale, int kv_format,
+                         const float* sink, const int32_t* idx, float softmax_scale,
+                         int64_t b, int64_t s, int h, int d, int64_t rows, int topk,
+                         void* o, void* workspace, size_t workspace_bytes, void* stream) {
+    if (kv_format != SA_KV_BF16 && kv_format != SA_KV_FP8_E4M3) return SA_ERR_INVALID_ARG;
+    if (b < 0 || s < 0 || h < 1 || d < 1 || rows < 0 || topk < 0) return SA_ERR_INVALID_ARG;
+    if (!supported_shape(b, s, h, d, rows, topk)) return SA_ERR_UNSUPPORTED;
+    if (kv_format == SA_KV_BF16 && kv_scale) return SA_ERR_INVALID_ARG;
+    if (b * s == 0) return SA_OK;  // nothing to compute; pointers of empty tensors may be NULL
+    // kv (and kv_scale) may be NULL only when there are no rows, idx only when topk == 0
+    if (!q || !sink || !o || (rows > 0 && !kv) || (topk > 0 && !idx)) return SA_ERR_INVALID_ARG;
+    if (kv_format == SA_KV_FP8_E4M3 && rows > 0 && !kv_scale) return SA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(o, 16) || !aligned(sink, 4) ||
+        !aligned(idx, 4))
+        return SA_ERR_INVALID_ARG;
+    const size_t need = sa_sparse_attn_workspace_size(b, s, h, d, rows, topk, kv_format);
+    if (!workspace || workspace_bytes < need) return SA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return SA_ERR_INVALID_ARG;
+    const size_t n_tok = (size_t)(b * s);
+    const size_t o_bytes = n_tok * h * (size_t)d * 2;
+    const size_t kv_bytes = (size_t)b * rows * d * (kv_format == SA_KV_BF16 ? 2 : 1);
+    if (overlaps(o, o_bytes, q, o_bytes) || overlaps(o, o_bytes, kv, kv_bytes) ||
+        overlaps(o, o_bytes, idx, n_tok * topk * 4) || overlaps(o, o_bytes, sink, h * 4) ||
+        overlaps(o, o_bytes, workspace, need) ||
+        (kv_scale && overlaps(o, o_bytes, kv_scale, (size_t)b * rows * (d / 32))))
+        return SA_ERR_INVALID_ARG;
+
+    sa::AttnCall c;
+    c.q = q;
+    c.kv = kv;
+    c.kv_scale = kv_scale;
+    c.kv_format = kv_format;
+    c.sink = sink;
+    c.idx = idx;
+    c.softmax_scale = softmax_scale;
+    c.b = b;
+    c.s = s;
+    c.h = h;
+    c.d = d;
+    c.rows = rows;
+    c.topk = topk;
+    c.o = o;
+    c.status = reinterpret_cast<uint32_t*>(workspace);
+    c.scratch = reinterpret_cast<uint8_t*>(workspace) + SA_STATUS_BYTES;
+    c.scratch_bytes = workspace_bytes - SA_STATUS_BYTES;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(sa::attn_mma_launch(c));
+}
+
+sa_status sa_window_idxs(int64_t start_pos, int64_t seqlen, int window, int32_t* idx, int64_t ld,
+                         int64_t nbatch, int64_t batch_stride, void* stream) {
+    if (window < 1 || seqlen < 0 || start_pos < 0 || nbatch < 0 || ld < window)
+        return SA_ERR_INVALID_ARG;
+    if (nbatch > 1 && batch_stride < seqlen * ld) return SA_ERR_INVALID_ARG;
+    if (start_pos > 0 && seqlen > 1) return SA_ERR_UNSUPPORTED;
+    if (seqlen == 0 || nbatch == 0) return SA_OK;
+    if (!idx || !aligned(idx, 4)) return SA_ERR_INVALID_ARG;
+    return from_cuda(sa::window_idxs_launch(start_pos, seqlen, window, idx, ld, nbatch,
+                                            batch_stride, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sa_act_quant_fp8(const void* x, int64_t n, int d, int64_t x_stride, void* x_rt,
+                           int64_t rt_stride, uint8_t* codes, int64_t codes_stride,
+                           uint8_t* scales, int64_t scales_stride, void* stream) {
+    if (n < 0 || d < 32 || d % 32 != 0) return SA_ERR_INVALID_ARG;
+    if (!x_rt && !codes && !scales) return SA_ERR_INVALID_ARG;
+    if (n == 0) return SA_OK;
+    if (!x || !aligned(x, 2) || x_stride < d) return SA_ERR_INVALID_ARG;
+    if (x_rt && (!aligned(x_rt, 2) || rt_stride < d)) return SA_ERR_INVALID_ARG;
+    if (codes && codes_stride < d) return SA_ERR_INVALID_ARG;
+    if (scales && scales_stride < d / 32) return SA_ERR_INVALID_ARG;
+    if (x_rt && x_rt != x && overlaps(x_rt, (size_t)((n - 1) * rt_stride + d) * 2, x,
+                                      (size_t)((n - 1) * x_stride + d) * 2))
+        return SA_ERR_INVALID_ARG;  // in place is allowed; a shifted overlap is not
+    if (x_rt == x && rt_stride != x_stride) return SA_ERR_INVALID_ARG;
+    return from_cuda(sa::act_quant_launch(x, n, d, x_stride, x_rt, rt_stride, codes, codes_stride,
+                                          scales, scales_stride,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sa_read_status(void* workspace, int clear, void* stream) {
+    if (!workspace || !aligned(workspace, 4)) return SA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && clear) {
+        e = cudaMemsetAsync(workspace, 0, sizeof word, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    if (e != cudaSuccess) return SA_ERR_CUDA;
+    if (word & sa::kStatusBadIndex) return SA_ERR_INDEX;
+    return SA_OK;
+}
+
+const char* sa_status_string(int status) {
+    switch (status) {
+        case SA_OK: return "ok";
+        case SA_ERR_INVALID_ARG: return "invalid argument";
+        case SA_ERR_UNSUPPORTED: return "unsupported shape or mode";
+        case SA_ERR_CUDA: return "CUDA error";
+        case SA_ERR_INDEX: return "index outside [-1, rows) seen";
+        case SA_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int sa_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// Internal declarations shared by the library's CUDA translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sparse_attn.h"
+
+namespace sa {
+
+// Status word bits (first 32-bit word of the workspace status block).
+constexpr uint32_t kStatusBadIndex = 1u;
+
+// Everything a sparse_attn kernel family needs for one call, already validated.
+struct AttnCall {
+    const void* q;
+    const void* kv;
+    const uint8_t* kv_scale;
+    int kv_format;
+    const float* sink;
+    const int32_t* idx;
+    float softmax_scale;
+    int64_t b, s;
+    int h, d;
+    int64_t rows;
+    int topk;
+    void* o;
+    uint32_t* status;   // device status word
+    void* scratch;      // workspace past the status block
+    size_t scratch_bytes;
+    cudaStream_t stream;
+};
+
+// mma.sync family (sa_attn_mma.cu)
+size_t attn_mma_scratch_bytes(int64_t b, int64_t s, int h, int d, int topk);
+cudaError_t attn_mma_launch(const AttnCall& c);
+
+// helpers (sa_helpers.cu)
+cudaError_t window_idxs_launch(int64_t start_pos, int64_t seqlen, int window, int32_t* idx,
+                               int64_t ld, int64_t nbatch, int64_t batch_stride,
+                               cudaStream_t stream);
+cudaError_t act_quant_launch(const void* x, int64_t n, int d, int64_t x_stride, void* x_rt,
+                             int64_t rt_stride, uint8_t* codes, int64_t codes_stride,
+                             uint8_t* scales, int64_t scales_stride, cudaStream_t stream);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace sa

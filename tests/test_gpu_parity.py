@@ -1,0 +1,280 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the CPU oracle on the same
+seeded inputs.  Indices and act_quant bit-exact; sparse_attn outputs within
+|gpu - oracle| <= 1e-2 + 1e-2 * |oracle| per element."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_latent_attention_gb300 as sa
+from sparse_latent_attention_gb300 import build, workloads
+from tests import _gpu
+from tests._helpers import assert_close_bf16, compose_idx_oracle
+
+pytestmark = pytest.mark.gpu
+
+ATOL = RTOL = 1e-2
+
+
+@pytest.fixture(scope="session")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    sa.load()
+    return torch.device("cuda:0")
+
+
+def _sample_tokens(wl, n, seed=0):
+    nt = wl.n_tokens
+    if nt <= n:
+        return np.arange(nt)
+    rng = np.random.default_rng(seed)
+    fixed = np.array([0, 1, 2, 63, 64, 127, 128, 129, nt // 2, nt - 2, nt - 1])
+    fixed = fixed[fixed < nt]
+    rest = rng.choice(nt, size=n - len(fixed), replace=False)
+    return np.unique(np.concatenate([fixed, rest]))
+
+
+def _oracle_on_tokens(wl, tokens, quantise):
+    tokens = np.asarray(tokens)
+    bsel = sorted(set((tokens // wl.s).tolist()))
+    kv_o, sc_o, idx = _gpu.oracle_inputs(wl, quantise, bsel)
+    q = wl.q[bsel]
+    idx_sel = idx[bsel]
+    pos = {b: i for i, b in enumerate(bsel)}
+    local = np.array([pos[t // wl.s] * wl.s + t % wl.s for t in tokens])
+    return oracle.sparse_attn(q, kv_o, wl.sink, idx_sel, wl.scale, kv_scales=sc_o,
+                              tokens=local), idx
+
+
+def _gpu_run(wl, dev, quantise):
+    x = _gpu.prepare(wl, dev, quantise)
+    ws = sa.new_workspace(wl.b, wl.s, wl.h, wl.d, wl.rows, wl.topk,
+                          sa.SA_KV_FP8_E4M3 if x["kv_scale"] is not None else sa.SA_KV_BF16,
+                          device=dev)
+    o = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, kv_scale=x["kv_scale"],
+                       workspace=ws)
+    torch.cuda.synchronize()
+    return o, x, ws
+
+
+# --------------------------------------------------------------------------------------------
+# helpers on the path: bit-exact
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("start_pos,seqlen,window,nbatch,ld", [
+    (0, 12, 8, 1, 8), (0, 4096, 128, 1, 128), (0, 300, 128, 2, 640), (0, 3, 8, 1, 8),
+    (12, 1, 8, 1, 8), (13, 1, 8, 3, 20), (5, 1, 8, 1, 8), (32768, 1, 128, 64, 1152),
+    (131072, 1, 128, 4, 2176), (1, 1, 1, 1, 1)])
+def test_window_idxs_bit_exact(dev, start_pos, seqlen, window, nbatch, ld):
+    out = torch.full((nbatch, seqlen, ld), -7, dtype=torch.int32, device=dev)
+    sa.window_idxs(start_pos, seqlen, window, out=out[:, :, :window], nbatch=nbatch)
+    got = out.cpu().numpy()
+    want = oracle.window_idxs(start_pos, seqlen, window)
+    for bi in range(nbatch):
+        assert (got[bi, :, :window] == want).all()
+        assert (got[bi, :, window:] == -7).all()  # nothing written past the window columns
+
+
+def _act_quant_inputs():
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((512, 512)).astype(np.float32)
+    # blocks spanning the whole bf16 range, exact zeros, tiny values near the 1e-4 floor,
+    # values on e4m3 rounding midpoints, negative zeros
+    x *= np.exp(rng.uniform(-80, 80, (512, 16))).repeat(32, axis=1).astype(np.float32)
+    x[0] = 0.0
+    x[1] = -0.0
+    x[2, :32] = 1e-4
+    x[3, :32] = 448.0 * np.array([1, 3.125 / 448, 1.0625 / 448, 17 / 448] * 8)
+    x[4] = rng.uniform(-1e-6, 1e-6, 512)
+    x[5, :] = 450.0
+    return workloads.to_bf16_bits(x)
+
+
+def test_act_quant_bit_exact(dev):
+    bits = _act_quant_inputs()
+    want_rt, want_codes, want_sc = oracle.act_quant(bits)
+    x = _gpu.u16_to_bf16_tensor(bits, dev)
+    rt = torch.empty_like(x)
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+    sc = torch.empty((x.shape[0], x.shape[1] // 32), dtype=torch.uint8, device=dev)
+    sa.act_quant_fp8(x, out_rt=rt, codes=codes, scales=sc)
+    assert (_gpu.bf16_tensor_to_u16(rt) == want_rt).all()
+    assert (codes.cpu().numpy() == want_codes).all()
+    assert (sc.cpu().numpy() == want_sc).all()
+    # in place, and rows strided inside a larger buffer (one ring slot per sequence)
+    y = x.clone()
+    sa.act_quant_fp8(y, out_rt=y)
+    assert (_gpu.bf16_tensor_to_u16(y) == want_rt).all()
+    cache = torch.zeros((512, 3, 512), dtype=torch.uint8, device=dev)
+    cscale = torch.zeros((512, 3, 16), dtype=torch.uint8, device=dev)
+    sa.act_quant_fp8(x, codes=cache[:, 1, :], scales=cscale[:, 1, :])
+    assert (cache[:, 1].cpu().numpy() == want_codes).all()
+    assert (cache[:, 0].cpu().numpy() == 0).all() and (cache[:, 2].cpu().numpy() == 0).all()
+    assert (cscale[:, 1].cpu().numpy() == want_sc).all()
+
+
+def test_act_quant_every_bf16_value(dev):
+    """Each of the 65536 bf16 patterns (NaN and inf excluded) inside a block with a fixed
+    amax, so every e4m3 rounding case and both signs are met."""
+    allv = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = (allv.astype(np.uint32) << 16).view(np.float32)
+    ok = np.isfinite(f)
+    vals = allv[ok]
+    for amax in (448.0, 1.0, 3e-3, 1e30):
+        fv = (vals.astype(np.uint32) << 16).view(np.float32)
+        keep = vals[np.abs(fv) <= amax]
+        n = (len(keep) + 30) // 31 * 31
+        blk = np.zeros(n, np.uint16)
+        blk[: len(keep)] = keep
+        blk = blk.reshape(-1, 31)
+        amax_bits = workloads.to_bf16_bits(np.float32([amax]))[0]
+        rows = np.concatenate([blk, np.full((blk.shape[0], 1), amax_bits, np.uint16)], axis=1)
+        rows = rows.reshape(-1, 64) if rows.shape[0] % 2 == 0 else np.concatenate(
+            [rows, np.zeros((1, 32), np.uint16)]).reshape(-1, 64)
+        want_rt, want_codes, want_sc = oracle.act_quant(rows)
+        x = _gpu.u16_to_bf16_tensor(rows, dev)
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        rt = torch.empty_like(x)
+        sc = torch.empty((x.shape[0], 2), dtype=torch.uint8, device=dev)
+        sa.act_quant_fp8(x, out_rt=rt, codes=codes, scales=sc)
+        assert (codes.cpu().numpy() == want_codes).all(), amax
+        assert (_gpu.bf16_tensor_to_u16(rt) == want_rt).all(), amax
+        assert (sc.cpu().numpy() == want_sc).all(), amax
+
+
+# --------------------------------------------------------------------------------------------
+# sparse_attn on the five named workloads (full size, sampled outputs)
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,n_sample", [("tiny", 16), ("swa_prefill", 64), ("cmp_prefill", 48),
+                                           ("decode", 64), ("fp8_decode", 24)])
+def test_named_workload_parity(dev, name, n_sample):
+    wl = workloads.make_named(name)
+    quantise = name != "tiny"
+    o, x, ws = _gpu_run(wl, dev, quantise)
+    assert sa.read_status(ws) == 0
+    # the whole index table matches the oracle's composition bit for bit
+    idx_want = compose_idx_oracle(wl)
+    assert (x["idx"].cpu().numpy() == idx_want).all()
+    tokens = _sample_tokens(wl, n_sample)
+    want, _ = _oracle_on_tokens(wl, tokens, quantise)
+    got = _gpu.bf16_tensor_to_u16(o.view(wl.n_tokens, wl.h, wl.d)[torch.from_numpy(tokens).to(dev)])
+    assert_close_bf16(got, want, ATOL, RTOL, what=name)
+    # properties over every output: finite, and zero exactly where a token lists no row
+    of = o.float()
+    assert torch.isfinite(of).all()
+    empty = (x["idx"] < 0).all(dim=-1)
+    if empty.any():
+        assert (of[empty] == 0).all()
+
+
+def test_bf16_round_trip_kv_matches_oracle(dev):
+    """The kv the attention reads for a named workload is the oracle's act_quant round trip."""
+    wl = workloads.make_named("swa_prefill")
+    kv = _gpu.device_kv_raw(wl, dev)
+    sa.act_quant_fp8(kv.view(-1, wl.d), out_rt=kv.view(-1, wl.d))
+    rt, _, _ = oracle.act_quant(wl.kv_raw_dense())
+    assert (_gpu.bf16_tensor_to_u16(kv) == rt).all()
+
+
+# --------------------------------------------------------------------------------------------
+# sparse_attn on small problems: every output compared
+# --------------------------------------------------------------------------------------------
+
+RANDOM_CASES = [
+    # b, s, h, d, rows, topk, extra
+    (2, 37, 64, 512, 300, 200, {}),                 # ragged tail over 4 tiles
+    (1, 9, 128, 512, 700, 650, {}),                 # two head blocks, 11 tiles
+    (3, 1, 64, 512, 5000, 1152, {}),                # decode: split idx columns + merge
+    (5, 1, 128, 512, 3000, 2176, {}),               # decode, 128 heads
+    (1, 20, 4, 64, 48, 16, {}),                     # tiny head count and head_dim
+    (2, 11, 100, 192, 90, 70, {}),                  # ragged heads, odd head_dim
+    (1, 13, 64, 256, 64, 64, dict(distinct=False)),  # repeated indices count repeatedly
+    (2, 7, 64, 512, 400, 130, dict(q_scale=12.0)),  # large logits: running max moves a lot
+    (1, 8, 64, 512, 100, 100, dict(sink_scale=30.0)),  # sinks far from the logits
+    (2, 9, 16, 128, 50, 40, dict(neg_frac=0.97)),   # nearly everything masked
+]
+
+
+@pytest.mark.parametrize("case", RANDOM_CASES, ids=lambda c: f"b{c[0]}s{c[1]}h{c[2]}d{c[3]}k{c[5]}")
+def test_random_parity(dev, case):
+    b, s, h, d, rows, topk, extra = case
+    wl = workloads.make_random(b, s, h, d, rows, topk, seed=1000 + b * 7 + s, all_neg_tokens=(1,),
+                               **extra)
+    o, x, ws = _gpu_run(wl, dev, quantise=False)
+    assert sa.read_status(ws) == 0
+    want = oracle.sparse_attn(wl.q, wl.kv_raw_dense(), wl.sink, compose_idx_oracle(wl), wl.scale)
+    assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what=str(case))
+    assert (_gpu.bf16_tensor_to_u16(o.view(-1, h, d)[1]) == 0).all()
+
+
+def test_sink_minus_inf_and_single_row(dev):
+    wl = workloads.make_random(2, 5, 64, 512, 40, 24, seed=77, neg_frac=0.0)
+    wl.sink[:] = -np.inf
+    wl.idx_tail[:] = -1
+    wl.idx_tail[..., 5] = 3
+    o, x, ws = _gpu_run(wl, dev, quantise=False)
+    kvd = wl.kv_raw_dense()
+    got = _gpu.bf16_tensor_to_u16(o)
+    for bi in range(2):
+        assert (got[bi] == kvd[bi, 3][None, None, :]).all()  # one row, no sink: that row exactly
+
+
+def test_empty_shapes(dev):
+    # topk == 0 and rows == 0: nothing listed, o == 0
+    for rows, topk in ((10, 0), (0, 7)):
+        wl = workloads.make_random(1, 4, 64, 512, max(rows, 1), topk, seed=5, neg_frac=1.0)
+        q = _gpu.u16_to_bf16_tensor(wl.q, dev)
+        kv = torch.zeros((1, rows, 512), dtype=torch.bfloat16, device=dev)
+        idx = torch.full((1, 4, topk), -1, dtype=torch.int32, device=dev)
+        sink = torch.from_numpy(wl.sink).to(dev)
+        o = torch.full_like(q, 3.0)
+        sa.sparse_attn(q, kv, sink, idx, wl.scale, out=o)
+        assert (o == 0).all()
+    # no tokens at all: a no-op
+    q = torch.empty((0, 4, 64, 512), dtype=torch.bfloat16, device=dev)
+    o = sa.sparse_attn(q, torch.zeros((0, 5, 512), dtype=torch.bfloat16, device=dev),
+                       torch.zeros(64, device=dev), torch.zeros((0, 4, 3), dtype=torch.int32,
+                                                                device=dev), 0.1)
+    assert o.shape == q.shape
+
+
+def test_out_of_range_index_is_flagged_and_ignored(dev):
+    wl = workloads.make_random(2, 6, 64, 512, 90, 70, seed=91)
+    x = _gpu.prepare(wl, dev, quantise=False)
+    idx_bad = x["idx"].clone()
+    idx_bad[0, 2, 5] = 90       # == rows
+    idx_bad[1, 4, 0] = -3
+    idx_bad[1, 5, 69] = 1 << 30
+    ws = sa.new_workspace(wl.b, wl.s, wl.h, wl.d, wl.rows, wl.topk, device=dev)
+    o = sa.sparse_attn(x["q"], x["kv"], x["sink"], idx_bad, wl.scale, workspace=ws)
+    assert sa.read_status(ws, clear=True) == sa._lib.SA_ERR_INDEX
+    assert sa.read_status(ws) == 0
+    idx_ok = idx_bad.clone()
+    idx_ok[(idx_ok < -1) | (idx_ok >= wl.rows)] = -1
+    want = oracle.sparse_attn(wl.q, wl.kv_raw_dense(), wl.sink, idx_ok.cpu().numpy(), wl.scale)
+    assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what="bad idx")
+
+
+@pytest.mark.parametrize("b,s,h,topk", [(2, 9, 64, 300), (4, 1, 128, 2176), (3, 1, 64, 1152)])
+def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk):
+    """Attention over e4m3 codes + e8m0 scales gives the same bits as attention over the bf16
+    round trip of the same rows (same kernel tiling and order)."""
+    wl = workloads.make_random(b, s, h, 512, 2500, topk, seed=300 + topk, kv_format="fp8")
+    raw = _gpu.device_kv_raw(wl, dev)
+    codes = torch.empty((b, wl.rows, 512), dtype=torch.uint8, device=dev)
+    scales = torch.empty((b, wl.rows, 16), dtype=torch.uint8, device=dev)
+    sa.act_quant_fp8(raw.view(-1, 512), codes=codes.view(-1, 512), scales=scales.view(-1, 16))
+    rt = raw.clone()
+    sa.act_quant_fp8(rt.view(-1, 512), out_rt=rt.view(-1, 512))
+    q = _gpu.u16_to_bf16_tensor(wl.q, dev)
+    sink = torch.from_numpy(wl.sink).to(dev)
+    idx = _gpu.device_idx(wl, dev)
+    o_fp8 = sa.sparse_attn(q, codes, sink, idx, wl.scale, kv_scale=scales)
+    o_bf16 = sa.sparse_attn(q, rt, sink, idx, wl.scale)
+    assert torch.equal(o_fp8.view(torch.int16), o_bf16.view(torch.int16))
