@@ -87,6 +87,35 @@ sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale,
 size_t sa_sparse_attn_workspace_size(int64_t b, int64_t s, int h, int d, int64_t rows, int topk,
                                      int kv_format);
 
+/* Size of the library's own scratch array used by sa_sparse_attn_static_scratch (64 MiB). */
+#define SA_STATIC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * sparse_attn without a caller workspace.  The source pages have no counterpart to this call: it
+ * exists for callers that cannot allocate device memory -- a plugin inside a host runtime that
+ * owns every device allocation and gives the plugin none, or a serving loop that must not call
+ * cudaMalloc / cudaFree (which can synchronise the device) on its request path.
+ *
+ * Computes exactly what sa_sparse_attn computes, with the same arguments apart from the
+ * workspace, which is replaced by a SA_STATIC_SCRATCH_BYTES array that the library keeps in
+ * device memory on every GPU that loads it, until the process exits.  Allocates nothing.
+ *   status_out  optional device uint32: receives the call's status word (bit 0 set when an index
+ *               outside [-1, rows) was seen); NULL to skip.  The word is cleared at the start of
+ *               every call.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current) and caches it: make that first call before any stream capture.  Every call
+ * shares the one array, which keeps the last call's contents; calls whose work overlaps on the
+ * GPU (unordered streams) race on it and must be serialised by the caller.
+ * Returns SA_ERR_WORKSPACE when the shape needs more scratch than SA_STATIC_SCRATCH_BYTES (only
+ * few-token calls with many idx columns need more than the status word), otherwise as
+ * sa_sparse_attn.
+ */
+sa_status sa_sparse_attn_static_scratch(const void* q, const void* kv, const uint8_t* kv_scale,
+                                        int kv_format, const float* sink, const int32_t* idx,
+                                        float softmax_scale, int64_t b, int64_t s, int h, int d,
+                                        int64_t rows, int topk, void* o, uint32_t* status_out,
+                                        void* stream);
+
 /*
  * Window index table (get_window_topk_idxs).
  *

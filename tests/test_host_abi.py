@@ -19,7 +19,8 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = _lib.declared_symbols()
     assert set(names) == {"sa_sparse_attn", "sa_sparse_attn_workspace_size", "sa_window_idxs",
-                          "sa_act_quant_fp8", "sa_read_status", "sa_status_string", "sa_version"}
+                          "sa_act_quant_fp8", "sa_read_status", "sa_status_string", "sa_version",
+                          "sa_sparse_attn_static_scratch"}
     for n in names:
         assert hasattr(lib, n), n
 
