@@ -33,7 +33,9 @@ typedef enum {
     SA_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement (see each call) */
     SA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     SA_ERR_INDEX = 4,        /* a kernel saw an index outside [-1, rows) (sa_read_status) */
-    SA_ERR_WORKSPACE = 5     /* workspace missing or smaller than the size query returned */
+    SA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than the size query returned */
+    SA_ERR_TIMEOUT = 6       /* a kernel's bounded wait gave up (sa_read_status); its output is
+                                not valid */
 } sa_status;
 
 typedef enum {
@@ -158,7 +160,8 @@ sa_status sa_act_quant_fp8(const void* x, int64_t n, int d, int64_t x_stride,
 
 /*
  * Reads the status word in a workspace (synchronises `stream` first) and returns SA_OK or the
- * first data error recorded there (SA_ERR_INDEX).  With clear != 0 the word is reset to zero.
+ * error recorded there: SA_ERR_TIMEOUT (a kernel wait gave up) before SA_ERR_INDEX (an index
+ * outside [-1, rows) was seen).  With clear != 0 the word is reset to zero.
  */
 sa_status sa_read_status(void* workspace, int clear, void* stream);
 

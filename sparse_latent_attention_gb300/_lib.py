@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsa.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "sparse_attn.h")
 
-SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_INDEX, SA_ERR_WORKSPACE = range(6)
+(SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_INDEX, SA_ERR_WORKSPACE,
+ SA_ERR_TIMEOUT) = range(7)
 SA_KV_BF16, SA_KV_FP8_E4M3 = 0, 1
 SA_STATUS_BYTES = 256
 

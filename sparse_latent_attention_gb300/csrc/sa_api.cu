@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "sa_internal.cuh"
 #include "sparse_attn.h"
@@ -30,6 +31,13 @@ bool supported_shape(int64_t b, int64_t s, int h, int d, int64_t rows, int topk)
 
 sa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SA_OK : SA_ERR_CUDA; }
 
+// SA_FORCE_MMA=1 in the environment routes every call to the mma.sync kernels (used to compare
+// the two kernel families on the same inputs); read on every call.
+bool force_mma() {
+    const char* v = getenv("SA_FORCE_MMA");
+    return v && v[0] == '1';
+}
+
 }  // namespace
 
 extern "C" {
@@ -38,7 +46,13 @@ size_t sa_sparse_attn_workspace_size(int64_t b, int64_t s, int h, int d, int64_t
                                      int kv_format) {
     if (kv_format != SA_KV_BF16 && kv_format != SA_KV_FP8_E4M3) return 0;
     if (!supported_shape(b, s, h, d, rows, topk)) return 0;
-    return SA_STATUS_BYTES + sa::align_up(sa::attn_mma_scratch_bytes(b, s, h, d, topk), 256);
+    // enough for either kernel family, whichever a call is routed to
+    size_t scratch = sa::attn_mma_scratch_bytes(b, s, h, d, topk);
+    if (sa::attn_tc_supports(h, d, kv_format)) {
+        const size_t tc_scratch = sa::attn_tc_scratch_bytes(b, s, h, topk);
+        if (tc_scratch > scratch) scratch = tc_scratch;
+    }
+    return SA_STATUS_BYTES + sa::align_up(scratch, 256);
 }
 
 sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale, int kv_format,
@@ -87,6 +101,8 @@ sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale,
     c.scratch = reinterpret_cast<uint8_t*>(workspace) + SA_STATUS_BYTES;
     c.scratch_bytes = workspace_bytes - SA_STATUS_BYTES;
     c.stream = reinterpret_cast<cudaStream_t>(stream);
+    if (sa::attn_tc_supports(h, d, kv_format) && !force_mma())
+        return from_cuda(sa::attn_tc_launch(c));
     return from_cuda(sa::attn_mma_launch(c));
 }
 
@@ -132,6 +148,7 @@ sa_status sa_read_status(void* workspace, int clear, void* stream) {
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     }
     if (e != cudaSuccess) return SA_ERR_CUDA;
+    if (word & sa::kStatusTimeout) return SA_ERR_TIMEOUT;
     if (word & sa::kStatusBadIndex) return SA_ERR_INDEX;
     return SA_OK;
 }
@@ -144,6 +161,7 @@ const char* sa_status_string(int status) {
         case SA_ERR_CUDA: return "CUDA error";
         case SA_ERR_INDEX: return "index outside [-1, rows) seen";
         case SA_ERR_WORKSPACE: return "workspace missing or too small";
+        case SA_ERR_TIMEOUT: return "a kernel wait gave up (pipeline stalled)";
         default: return "unknown status";
     }
 }

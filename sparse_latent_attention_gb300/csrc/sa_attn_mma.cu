@@ -502,8 +502,15 @@ cudaError_t attn_mma_launch(const AttnCall& c) {
     dim3 grid((unsigned)n_tokens, g.n_splits, g.hblocks);
     cudaError_t e = c.kv_format == SA_KV_BF16 ? launch_d<false>(c, p, grid) : launch_d<true>(c, p, grid);
     if (e != cudaSuccess || g.n_splits == 1) return e;
-    attn_combine_kernel<<<(unsigned)n_tokens, dim3(32, 8), 0, c.stream>>>(
-        p.part_ml, p.part_o, c.sink, p.o, c.h, c.d, g.n_splits);
+    return attn_combine_launch(p.part_ml, p.part_o, c.sink, p.o, n_tokens, c.h, c.d, g.n_splits,
+                               c.stream);
+}
+
+cudaError_t attn_combine_launch(const float* part_ml, const float* part_o, const float* sink,
+                                void* o, int64_t n_tokens, int h, int d, int n_splits,
+                                cudaStream_t stream) {
+    attn_combine_kernel<<<(unsigned)n_tokens, dim3(32, 8), 0, stream>>>(
+        part_ml, part_o, sink, reinterpret_cast<__nv_bfloat16*>(o), h, d, n_splits);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,844 @@
+// sparse_attn on the 5th-generation tensor cores (tcgen05, accumulators in TMEM), head_dim 512.
+//
+// Source: "Module attn" API page (spark_model, deepseek_v41_ref/attn), Functions: sparse_attn
+// and the precision paragraph; "DeepSeek V4.1" attention page, Attention.forward.
+//
+// Formulation.  All heads of a query token read the same gathered kv rows, and the rows serve as
+// both keys and values.  With head_dim 512 an f32 accumulator of O for 64 heads needs 256 TMEM
+// columns in any orientation, while with heads as the MMA's M dimension O takes all 512 columns
+// (the full TMEM) and leaves no room for the logits.  So the gathered rows are the M dimension:
+//   S^T[128 rows x 64 heads]  = KV_tile[128 x 512] . Q^T            (4 x 8 MMAs, K = 512)
+//   O^T[512 x 64 heads]      += KV_tile^T[512 x 128] . P^T[128 x 64] (4 M-chunks x 8 MMAs)
+// TMEM holds O^T (256 columns) and two S^T buffers (2 x 64).  The same swizzled shared-memory
+// tile is the K-major A operand of the first product and the MN-major A operand of the second.
+// The softmax runs down the columns of S^T (one TMEM lane = one gathered row per thread): the
+// column maximum is a warp max reduction plus a 4-warp exchange, and a running maximum is only
+// raised (and O rescaled) when a new logit exceeds it by more than 2^8, so the rescale is rare.
+// The sink joins the denominator once, in the epilogue: o = O / (l + 2^(sink log2e - m)).
+//
+// Roles (persistent CTAs, one 64-head block of one query token per task, 384 threads):
+//   warp 0      MMA issue (one thread) and TMEM allocation
+//   warp 1      Q loads (TMA, 128-byte swizzle)
+//   warps 2-3   kv row gather (cp.async 16 B, swizzled in place; rows already resident from the
+//               previous tile are kept -- see below)
+//   warps 4-7   softmax: S^T -> P^T (bf16, shared memory), running max, O rescale
+//   warps 8-11  epilogue: O^T -> o (bf16) or split partials
+// Every wait is bounded; a wait that gives up raises the timeout bit and every role unwinds.
+//
+// Row placement.  The order of the gathered rows inside a tile does not matter (the softmax and
+// P.V sum over rows; masking uses the recorded row id of each slot).  When the valid rows of a
+// tile have distinct residues mod 128, row j goes to slot j mod 128; otherwise row r of the tile
+// goes to slot r.  A row already sitting in its slot from the previous tile is not copied again.
+// A CTA takes a contiguous block of tasks, so consecutive query tokens of a sliding window (127
+// of 128 rows shared) reload one row per token.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "sa_internal.cuh"
+#include "sa_tc.cuh"
+
+namespace sa {
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 512;           // head_dim handled by this kernel
+constexpr int kRows = 128;        // gathered rows per tile (MMA M)
+constexpr int kHeads = 64;        // heads per task (MMA N)
+constexpr int kGroups = 4;        // 128-wide d groups (pipeline granularity)
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// Shared-memory map (dynamic, 1024-byte aligned base)
+constexpr uint32_t kKvBytes = kRows * kD * 2;     // 128 KB: 8 blocks of [128 rows x 128 B]
+constexpr uint32_t kQBytes = kHeads * kD * 2;     // 64 KB: 8 blocks of [64 heads x 128 B]
+constexpr uint32_t kPBytes = kRows * kHeads * 2;  // 16 KB: [128 rows x 128 B]
+constexpr uint32_t kOffKv = 0;
+constexpr uint32_t kOffQ = kOffKv + kKvBytes;
+constexpr uint32_t kOffP = kOffQ + kQBytes;
+constexpr uint32_t kStageBytes = 32 * kRows * 2;  // 8 KB: o staging [32 heads x 128 d]
+constexpr uint32_t kOffStage = kOffP + kPBytes;
+constexpr uint32_t kOffMisc = kOffStage + kStageBytes;
+
+struct Misc {
+    uint64_t q_full[kGroups], q_empty[kGroups];
+    uint64_t kv_full[kGroups], kv_empty[kGroups];
+    uint64_t s_full[2], s_empty[2];
+    uint64_t p_full, p_empty;
+    uint64_t o_full, o_empty[kGroups];
+    uint64_t stats_full[2];
+    uint64_t sm_bar, ep_bar, pr_bar, done;
+    uint32_t tmem_base;
+    int abort;
+    int need_corr[2];
+    int row_id[2][kRows];              // kv row held by each slot per tile parity, -1 = none
+    uint32_t ring_bits[2][4];          // residues mod 128 of a tile's valid rows
+    int ring_count[2];                 // number of valid rows of a tile
+    int64_t tile_seq[2];               // sequence whose rows a tile holds (-1 = none)
+    int2 copy_list[2][64];             // per producer warp: (kv row, slot) of the rows to copy
+    float colred[4][kHeads];           // per-warp column max of the current tile
+    float colsum[4][kHeads];           // per-warp column sums of p of the last tile
+    float l[kHeads];                   // running sum of p (up to the last fold)
+    float m[kHeads];                   // running max (log2 units)
+    float mu[kHeads];                  // the running max with -inf replaced by 0
+    float alpha[kHeads];               // rescale factor of this tile
+    float stats_m[2][kHeads];          // final max (0 when none) per task parity
+    float stats_l[2][kHeads];          // final sum per task parity
+    alignas(16) float inv[2][kHeads];  // epilogue: 1 / denominator per task parity
+};
+constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Params {
+    const __nv_bfloat16* kv;
+    const void* zero_src;  // any valid 16-byte aligned address: source of zero-byte copies
+    const float* sink;
+    const int32_t* idx;
+    __nv_bfloat16* o;
+    float* part_ml;
+    float* part_o;
+    uint32_t* status;
+    float scale_log2;
+    int64_t s_len;
+    int h;
+    int hblocks;
+    int64_t rows;
+    int topk;
+    int n_tiles;
+    int n_splits;
+    int tiles_per_split;
+    int64_t n_tasks;
+};
+
+struct Task {
+    int64_t token;
+    int hb, split, t0, t1;
+};
+
+// Tasks [begin, end) of this CTA: a contiguous block, so that consecutive query tokens of one
+// sequence (which share most window rows) run back to back on the same SM.
+__device__ __forceinline__ void task_range(const Params& p, int64_t& begin, int64_t& end) {
+    const int64_t g = gridDim.x, i = blockIdx.x;
+    const int64_t base = p.n_tasks / g, rem = p.n_tasks % g;
+    begin = i * base + (i < rem ? i : rem);
+    end = begin + base + (i < rem ? 1 : 0);
+}
+
+__device__ __forceinline__ Task task_of(const Params& p, int64_t tau) {
+    Task t;
+    t.split = (int)(tau % p.n_splits);
+    const int64_t th = tau / p.n_splits;
+    t.hb = (int)(th % p.hblocks);
+    t.token = th / p.hblocks;
+    t.t0 = t.split * p.tiles_per_split;
+    t.t1 = min(p.n_tiles, t.t0 + p.tiles_per_split);
+    if (t.t1 < t.t0) t.t1 = t.t0;
+    return t;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Warp reduce-scatter over 64 values per lane: afterwards lane l holds the reduction over the
+// warp of heads 2l and 2l+1 in out0 / out1.
+template <bool kMax>
+__device__ __forceinline__ void warp_reduce_scatter64(const float (&x)[64], int lane, float& out0,
+                                                      float& out1) {
+    float a[32];
+    {
+        const bool hi = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float send = hi ? x[i] : x[32 + i];
+            const float keep = hi ? x[32 + i] : x[i];
+            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+            a[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+    float b[16];
+    {
+        const bool hi = lane & 8;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float send = hi ? a[i] : a[16 + i];
+            const float keep = hi ? a[16 + i] : a[i];
+            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+            b[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+    float c[8];
+    {
+        const bool hi = lane & 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float send = hi ? b[i] : b[8 + i];
+            const float keep = hi ? b[8 + i] : b[i];
+            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+            c[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+    float e[4];
+    {
+        const bool hi = lane & 2;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float send = hi ? c[i] : c[4 + i];
+            const float keep = hi ? c[4 + i] : c[i];
+            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+            e[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+    {
+        const bool hi = lane & 1;
+        float f[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float send = hi ? e[i] : e[2 + i];
+            const float keep = hi ? e[2 + i] : e[i];
+            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+            f[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+        out0 = f[0];
+        out1 = f[1];
+    }
+}
+
+// Barrier among the 128 threads of one warpgroup, on an mbarrier so that it is bounded.
+__device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t& phase, volatile int* abort) {
+    mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase & 1, abort);
+    ++phase;
+    return ok;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap q_map, Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    Misc& M = *reinterpret_cast<Misc*>(smem + kOffMisc);
+    const uint32_t s_kv = smem_addr(smem + kOffKv);
+    const uint32_t s_q = smem_addr(smem + kOffQ);
+    const uint32_t s_p = smem_addr(smem + kOffP);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int* abort = &M.abort;
+
+    if (tid == 0) {
+        for (int g = 0; g < kGroups; ++g) {
+            mbar_init(smem_addr(&M.q_full[g]), 1);
+            mbar_init(smem_addr(&M.q_empty[g]), 1);
+            mbar_init(smem_addr(&M.kv_full[g]), 64);
+            mbar_init(smem_addr(&M.kv_empty[g]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&M.s_full[b]), 1);
+            mbar_init(smem_addr(&M.s_empty[b]), 128);
+            mbar_init(smem_addr(&M.stats_full[b]), 1);
+        }
+        mbar_init(smem_addr(&M.p_full), 128);
+        mbar_init(smem_addr(&M.p_empty), 1);
+        mbar_init(smem_addr(&M.o_full), 1);
+        for (int c = 0; c < kGroups; ++c) mbar_init(smem_addr(&M.o_empty[c]), 128);
+        mbar_init(smem_addr(&M.sm_bar), 128);
+        mbar_init(smem_addr(&M.ep_bar), 128);
+        mbar_init(smem_addr(&M.pr_bar), 64);
+        mbar_init(smem_addr(&M.done), 1);
+        M.abort = 0;
+        M.need_corr[0] = M.need_corr[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_addr(&M.tmem_base), 512);
+        tmem_relinquish();
+    }
+    // every slot starts as a finite (zero) row that no tile claims
+    for (int i = tid; i < 2 * kRows; i += kThreads) (&M.row_id[0][0])[i] = -1;
+    if (tid < 8) (&M.ring_bits[0][0])[tid] = 0;
+    if (tid < 2) {
+        M.ring_count[tid] = 0;
+        M.tile_seq[tid] = -1;
+    }
+    for (uint32_t i = tid; i < kKvBytes / 16; i += kThreads)
+        reinterpret_cast<uint4*>(smem + kOffKv)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 1 && lane == 0) tma_prefetch_desc(&q_map);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = M.tmem_base;
+    int64_t tb, te;
+    task_range(p, tb, te);
+
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16_f32(kRows, kHeads, false, false);
+            constexpr uint32_t id_o = idesc_bf16_f32(kRows, kHeads, true, true);
+            // base descriptors; the per-instruction ones add a start-address offset (>> 4)
+            const uint64_t a_s0 = smem_desc_sw128(s_kv, 16, 1024);
+            const uint64_t b_s0 = smem_desc_sw128(s_q, 16, 1024);
+            const uint64_t a_o0 = smem_desc_sw128(s_kv, 16384, 1024);
+            const uint64_t b_o0 = smem_desc_sw128(s_p, 8192, 1024);
+            uint32_t T = 0;
+            int64_t k = 0;
+            bool ok = true;
+            for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
+                const Task t = task_of(p, tau);
+                const uint32_t kp = (uint32_t)(k & 1);
+                if (t.t0 == t.t1) {  // nothing listed for this task: keep every phase in step
+                    for (int g = 0; g < kGroups && ok; ++g) {
+                        ok = mbar_wait(smem_addr(&M.q_full[g]), kp, abort);
+                        mma_commit(smem_addr(&M.q_empty[g]));
+                    }
+                    for (int c = 0; c < kGroups && ok; ++c)
+                        ok = mbar_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort);
+                    mma_commit(smem_addr(&M.o_full));
+                    continue;
+                }
+                for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
+                    const uint32_t b = T & 1, use = (T >> 1) & 1, tp = T & 1;
+                    const uint32_t s_col = tmem + 256 + 64 * b;
+                    ok = mbar_wait(smem_addr(&M.s_empty[b]), use ^ 1, abort);
+                    for (int g = 0; g < kGroups && ok; ++g) {
+                        ok = mbar_wait(smem_addr(&M.kv_full[g]), tp, abort);
+                        if (ok && ti == t.t0) ok = mbar_wait(smem_addr(&M.q_full[g]), kp, abort);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // K steps of 16 inside a 128-byte row advance the start address by 32 B
+                        // (2 in the descriptor's 16-byte units); the second 64-wide block of the
+                        // group is 16 KB further in the kv tile and 8 KB further in Q
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint64_t a = a_s0 + (uint64_t)(g * 2048 + (ks >> 2) * 1024 + (ks & 3) * 2);
+                            const uint64_t bq = b_s0 + (uint64_t)(g * 1024 + (ks >> 2) * 512 + (ks & 3) * 2);
+                            mma_bf16_ss(s_col, a, bq, id_s, (g | ks) != 0);
+                        }
+                        if (ti == t.t1 - 1) mma_commit(smem_addr(&M.q_empty[g]));
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_addr(&M.s_full[b]));
+                    ok = mbar_wait(smem_addr(&M.p_full), tp, abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int c = 0; c < kGroups && ok; ++c) {
+                        if (ti == t.t0) {  // the epilogue has read this chunk of the last task's O
+                            ok = mbar_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {  // 16 rows = 2 KB per K step
+                            const uint64_t a = a_o0 + (uint64_t)(c * 2048 + ks * 128);
+                            const uint64_t bp = b_o0 + (uint64_t)(ks * 128);
+                            mma_bf16_ss(tmem + 64 * c, a, bp, id_o, !(ti == t.t0 && ks == 0));
+                        }
+                        mma_commit(smem_addr(&M.kv_empty[c]));
+                    }
+                    mma_commit(smem_addr(&M.p_empty));
+                    if (ti == t.t1 - 1) mma_commit(smem_addr(&M.o_full));
+                }
+            }
+            // let every issued MMA finish before the accumulators are released
+            mma_commit(smem_addr(&M.done));
+            mbar_wait(smem_addr(&M.done), 0, abort);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ Q loads (TMA)
+        if (lane == 0) {
+            int64_t k = 0;
+            bool ok = true;
+            for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
+                const Task t = task_of(p, tau);
+                const int32_t y = (int32_t)(t.token * p.h + (int64_t)t.hb * kHeads);
+                for (int g = 0; g < kGroups && ok; ++g) {
+                    ok = mbar_wait(smem_addr(&M.q_empty[g]), (uint32_t)(k & 1) ^ 1, abort);
+                    if (!ok) break;
+                    const uint32_t bar = smem_addr(&M.q_full[g]);
+                    mbar_arrive_expect_tx(bar, 2 * 8192);
+                    tma_load_2d(s_q + (2 * g) * 8192, &q_map, 128 * g, y, bar);
+                    tma_load_2d(s_q + (2 * g + 1) * 8192, &q_map, 128 * g + 64, y, bar);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------------ kv gather
+        const int pw = warp - 2;       // producer warp 0 / 1
+        const int pt_id = tid - 64;    // 0 .. 63
+        uint32_t T = 0, pr_phase = 0;
+        bool ok = true;
+        for (int64_t tau = tb; tau < te && ok; ++tau) {
+            const Task t = task_of(p, tau);
+            const int64_t bi = t.token / p.s_len;
+            const int32_t* idx_tok = p.idx + t.token * (int64_t)p.topk;
+            const __nv_bfloat16* kvb = p.kv + bi * p.rows * (int64_t)kD;
+            for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
+                const uint32_t tp = T & 1;
+                // the two tile rows this thread resolves: r = pt_id and pt_id + 64
+                int jr[2];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int col = ti * kRows + pt_id + 64 * hf;
+                    int j = col < p.topk ? __ldg(idx_tok + col) : -1;
+                    if (j < -1 || j >= p.rows) {
+                        atomicOr(p.status, kStatusBadIndex);
+                        j = -1;
+                    }
+                    jr[hf] = j;
+                }
+                // placement: ring (slot = j mod 128) when the valid rows' residues are distinct
+                M.row_id[tp][pt_id] = -1;
+                M.row_id[tp][pt_id + 64] = -1;
+                int nvalid = 0;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                    if (jr[hf] >= 0) {
+                        atomicOr(&M.ring_bits[tp][(jr[hf] & 127) >> 5], 1u << (jr[hf] & 31));
+                        ++nvalid;
+                    }
+                if (nvalid) atomicAdd(&M.ring_count[tp], nvalid);
+                if (pt_id == 0) M.tile_seq[tp] = bi;
+                if (!(ok = wg_sync(smem_addr(&M.pr_bar), pr_phase, abort))) break;
+                // a slot's row can be kept only if it belongs to this same sequence
+                const bool same_seq = M.tile_seq[tp ^ 1] == bi;
+                const bool ring = __popc(M.ring_bits[tp][0]) + __popc(M.ring_bits[tp][1]) +
+                                      __popc(M.ring_bits[tp][2]) + __popc(M.ring_bits[tp][3]) ==
+                                  M.ring_count[tp];
+                int slot[2];
+                bool copy[2];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int j = jr[hf];
+                    slot[hf] = ring ? (j & 127) : pt_id + 64 * hf;
+                    copy[hf] = j >= 0 && (!same_seq || M.row_id[tp ^ 1][slot[hf]] != j);
+                    if (j >= 0) M.row_id[tp][slot[hf]] = j;
+                }
+                if (pt_id == 0) {  // the next tile (other parity) starts from a clean slate
+                    M.ring_bits[tp ^ 1][0] = M.ring_bits[tp ^ 1][1] = 0;
+                    M.ring_bits[tp ^ 1][2] = M.ring_bits[tp ^ 1][3] = 0;
+                    M.ring_count[tp ^ 1] = 0;
+                }
+                // the rows this warp copies, compacted into a list (ballot prefix counts)
+                const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, copy[0]);
+                const uint32_t m1 = __ballot_sync(0xFFFFFFFFu, copy[1]);
+                const uint32_t below = (1u << lane) - 1u;
+                const int n0 = __popc(m0), ncopy = n0 + __popc(m1);
+                if (copy[0]) M.copy_list[pw][__popc(m0 & below)] = make_int2(jr[0], slot[0]);
+                if (copy[1]) M.copy_list[pw][n0 + __popc(m1 & below)] = make_int2(jr[1], slot[1]);
+                __syncwarp();
+                for (int g = 0; g < kGroups && ok; ++g) {
+                    ok = mbar_wait(smem_addr(&M.kv_empty[g]), tp ^ 1, abort);
+                    if (!ok) break;
+                    const int u = 16 * g + (lane & 15);  // 16-byte unit of the 1 KB row
+#pragma unroll 4
+                    for (int e = lane >> 4; e < ncopy; e += 2) {  // two rows per instruction
+                        const int2 jr_s = M.copy_list[pw][e];
+                        const int r = jr_s.y;
+                        const uint32_t dst =
+                            s_kv + (u >> 3) * 16384 + r * 128 + ((((u & 7) ^ (r & 7)) & 7) << 4);
+                        cp_async16(dst, kvb + (int64_t)jr_s.x * kD + u * 8, 16u);
+                    }
+                    cp_async_commit();
+                }
+                if (!ok) break;
+                // every group is in flight; publish them in order as they land
+                cp_async_wait<3>();
+                fence_proxy_async_smem();
+                mbar_arrive(smem_addr(&M.kv_full[0]));
+                cp_async_wait<2>();
+                fence_proxy_async_smem();
+                mbar_arrive(smem_addr(&M.kv_full[1]));
+                cp_async_wait<1>();
+                fence_proxy_async_smem();
+                mbar_arrive(smem_addr(&M.kv_full[2]));
+                cp_async_wait<0>();
+                fence_proxy_async_smem();
+                mbar_arrive(smem_addr(&M.kv_full[3]));
+            }
+        }
+        cp_async_wait<0>();
+    } else if (warp < 8) {
+        // ------------------------------------------------------------------ softmax
+        // Per tile: column max of the logits -> running max m (raised only past the threshold),
+        // p = 2^(x - m) written as P^T, and the tile's column sums; the sums are folded into the
+        // running l = alpha * l + sum at the next tile (and once more at the end of the task).
+        const int q4 = warp & 3;
+        const int row = 32 * q4 + lane;  // TMEM lane = tile row
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        uint32_t T = 0, sm_phase = 0;
+        int64_t k = 0;
+        bool ok = true;
+        for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
+            const Task t = task_of(p, tau);
+            const int kpar = (int)(k & 1);
+            for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
+                const uint32_t b = T & 1, use = (T >> 1) & 1, tp = T & 1;
+                const bool first = ti == t.t0;
+                ok = mbar_wait(smem_addr(&M.kv_full[0]), tp, abort);
+                if (ok) ok = mbar_wait(smem_addr(&M.s_full[b]), use, abort);
+                if (!ok) break;
+                const bool valid = M.row_id[tp][row] >= 0;
+                const uint32_t s_addr = tmem + lane_base + 256 + 64 * b;
+                tc_fence_after();
+                // pass 1: column maximum of the scaled logits over the 128 rows
+                {
+                    float x[64];
+                    {
+                        uint32_t r[64];
+                        tmem_ld_32x32b_x64(s_addr, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int h = 0; h < 64; ++h)
+                            x[h] = valid ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
+                    }
+#pragma unroll
+                    for (int h = 0; h < 64; ++h) {  // warp max per head, one lane stores it
+                        float mx;
+                        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(x[h]));
+                        if (lane == (h & 31)) M.colred[q4][h] = mx;
+                    }
+                }
+                if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
+                if (row < kHeads) {
+                    const int h = row;
+                    if (!first)  // fold the previous tile's column sums
+                        M.l[h] = M.alpha[h] * M.l[h] + (M.colsum[0][h] + M.colsum[1][h]) +
+                                 (M.colsum[2][h] + M.colsum[3][h]);
+                    const float cm = fmaxf(fmaxf(M.colred[0][h], M.colred[1][h]),
+                                           fmaxf(M.colred[2][h], M.colred[3][h]));
+                    const float mo = M.m[h];
+                    float mn, al = 1.f;
+                    if (first) {
+                        mn = cm;
+                        al = 0.f;  // the first fold starts l from this tile's sum
+                        M.l[h] = 0.f;
+                    } else {
+                        mn = cm > mo + kRescaleThreshold ? cm : mo;
+                        if (mn != mo) {
+                            al = fast_exp2(mo - mn);  // 0 when mo = -inf (nothing summed yet)
+                            M.need_corr[tp] = 1;
+                        }
+                    }
+                    M.m[h] = mn;
+                    M.mu[h] = mn == -INFINITY ? 0.f : mn;
+                    M.alpha[h] = al;
+                }
+                if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
+                const bool corr = !first && M.need_corr[tp];
+                if (row == 0) M.need_corr[tp ^ 1] = 0;
+
+                // P buffer free and the previous PV done (O stable)
+                ok = mbar_wait(smem_addr(&M.p_empty), tp ^ 1, abort);
+                if (!ok) break;
+                if (corr) {
+                    tc_fence_after();
+                    for (int c = 0; c < 2 * kGroups; ++c) {
+                        uint32_t r[32];
+                        const uint32_t ta = tmem + lane_base + 32 * c;  // heads 32 (c & 1) ..
+                        tmem_ld_32x32b_x32(ta, r);
+                        tmem_wait_ld();
+                        const float* al = &M.alpha[32 * (c & 1)];
+#pragma unroll
+                        for (int h = 0; h < 32; ++h)
+                            r[h] = __float_as_uint(__uint_as_float(r[h]) * al[h]);
+                        tmem_st_32x32b_x32(ta, r);
+                    }
+                    tmem_wait_st();
+                }
+                // pass 2: p = 2^(x - m), the P^T row (128-byte swizzled MN-major operand)
+                float pr[64];
+                {
+                    uint32_t r[64];
+                    tmem_ld_32x32b_x64(s_addr, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int h = 0; h < 64; ++h)
+                        pr[h] = valid ? fast_exp2(__uint_as_float(r[h]) * p.scale_log2 - M.mu[h])
+                                      : 0.f;
+                }
+                tc_fence_before();
+                mbar_arrive(smem_addr(&M.s_empty[b]));
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t dst = s_p + row * 128 + ((((uint32_t)u ^ (row & 7)) & 7) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                                 "r"(pack_bf16(pr[8 * u], pr[8 * u + 1])),
+                                 "r"(pack_bf16(pr[8 * u + 2], pr[8 * u + 3])),
+                                 "r"(pack_bf16(pr[8 * u + 4], pr[8 * u + 5])),
+                                 "r"(pack_bf16(pr[8 * u + 6], pr[8 * u + 7]))
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(smem_addr(&M.p_full));
+                // this tile's column sums, folded in at the next tile / the end of the task
+                {
+                    float s0, s1;
+                    warp_reduce_scatter64<false>(pr, lane, s0, s1);
+                    M.colsum[q4][2 * lane] = s0;
+                    M.colsum[q4][2 * lane + 1] = s1;
+                }
+            }
+            if (!ok) break;
+            // final statistics of the task
+            if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
+            if (row < kHeads) {
+                const int h = row;
+                float l = 0.f, mh = -INFINITY;
+                if (t.t1 > t.t0) {
+                    l = M.alpha[h] * M.l[h] + (M.colsum[0][h] + M.colsum[1][h]) +
+                        (M.colsum[2][h] + M.colsum[3][h]);
+                    mh = M.m[h];
+                }
+                M.stats_l[kpar][h] = l;
+                M.stats_m[kpar][h] = mh == -INFINITY ? 0.f : mh;
+            }
+            if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
+            if (row == 0) mbar_arrive(smem_addr(&M.stats_full[kpar]));
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        // O^T chunk c (128 d x 64 heads) leaves TMEM at once (the MMA may refill it); the bf16
+        // values go through a [32 heads x 128 d] shared-memory stage so that o is written as
+        // 256-byte runs with 16-byte stores.  Every thread passes every barrier of a task, even
+        // after a failed wait, so the warpgroup's barriers never split.
+        const int q4 = warp & 3;
+        const int et = tid - 256;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        const uint32_t s_stage = smem_addr(smem + kOffStage);
+        int64_t k = 0;
+        bool ok = true;
+        for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
+            const Task t = task_of(p, tau);
+            const int kpar = (int)(k & 1);
+            const int h0 = t.hb * kHeads;
+            const int hc = min(kHeads, p.h - h0);
+            ok = mbar_wait(smem_addr(&M.o_full), (uint32_t)kpar, abort);
+            if (ok) ok = mbar_wait(smem_addr(&M.stats_full[kpar]), (uint32_t)((k >> 1) & 1), abort);
+            tc_fence_after();
+            const bool split = p.n_splits > 1;
+            const int64_t pbase = (t.token * p.n_splits + t.split) * (int64_t)p.h + h0;
+            if (et < kHeads) {
+                const int h = et;
+                const float l = M.stats_l[kpar][h], mu = M.stats_m[kpar][h];
+                float inv = 0.f;
+                if (ok && h < hc) {
+                    if (split) {
+                        p.part_ml[(pbase + h) * 2 + 0] = mu;
+                        p.part_ml[(pbase + h) * 2 + 1] = l;
+                    } else if (l > 0.f) {
+                        inv = 1.f / (l + fast_exp2(p.sink[h0 + h] * kLog2e - mu));
+                    }
+                }
+                M.inv[kpar][h] = inv;
+            }
+            named_barrier(1, 128);
+            for (int c = 0; c < kGroups; ++c) {
+                uint32_t r[64];
+                tmem_ld_32x32b_x64(tmem + lane_base + 64 * c, r);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(smem_addr(&M.o_empty[c]));
+                const int dl = 32 * q4 + lane;  // d within the chunk
+                if (split) {
+                    if (ok) {
+                        float* po = p.part_o + pbase * kD + 128 * c + dl;
+#pragma unroll
+                        for (int h = 0; h < 64; ++h)
+                            if (h < hc) po[(int64_t)h * kD] = __uint_as_float(r[h]);
+                    }
+                    continue;
+                }
+#pragma unroll
+                for (int rh = 0; rh < 2; ++rh) {
+                    float iv[32];
+#pragma unroll
+                    for (int v4 = 0; v4 < 8; ++v4) {
+                        const float4 f = *reinterpret_cast<const float4*>(&M.inv[kpar][32 * rh + 4 * v4]);
+                        iv[4 * v4] = f.x;
+                        iv[4 * v4 + 1] = f.y;
+                        iv[4 * v4 + 2] = f.z;
+                        iv[4 * v4 + 3] = f.w;
+                    }
+                    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffStage);
+#pragma unroll
+                    for (int hl = 0; hl < 32; ++hl) {
+                        const float v = iv[hl] > 0.f ? __uint_as_float(r[32 * rh + hl]) * iv[hl] : 0.f;
+                        stage[hl * 128 + dl] = __float2bfloat16_rn(v);
+                    }
+                    named_barrier(1, 128);
+                    if (ok) {
+#pragma unroll
+                        for (int it = 0; it < 4; ++it) {
+                            const int hl = 8 * q4 + 2 * it + (lane >> 4);
+                            const int h = 32 * rh + hl;
+                            if (h < hc) {
+                                uint4 v;
+                                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                             : "r"(s_stage + hl * 256 + (lane & 15) * 16));
+                                *reinterpret_cast<uint4*>(p.o + (t.token * p.h + h0 + h) * (int64_t)kD +
+                                                          128 * c + (lane & 15) * 8) = v;
+                            }
+                        }
+                    }
+                    named_barrier(1, 128);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && M.abort) atomicOr(p.status, kStatusTimeout);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &f, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+int sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev < 64 && counts[dev]) return counts[dev];
+    int n = 148;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (dev < 64) counts[dev] = n;
+    return n;
+}
+
+struct TcGeometry {
+    int n_tiles, hblocks, n_splits, tiles_per_split;
+};
+
+// Split the idx columns of a token over several tasks only when the tokens alone cannot fill
+// the GPU (decode); the split count is device-independent so the workspace size is too.
+TcGeometry tc_geometry(int64_t n_tokens, int h, int topk) {
+    constexpr int kAssumedSms = 152;
+    TcGeometry g;
+    g.n_tiles = (topk + kRows - 1) / kRows;
+    g.hblocks = (h + kHeads - 1) / kHeads;
+    const int64_t base = n_tokens * g.hblocks;
+    int splits = 1;
+    if (g.n_tiles > 1 && base < kAssumedSms) {
+        splits = (int)(kAssumedSms / base);
+        if (splits > g.n_tiles) splits = g.n_tiles;
+        if (splits < 1) splits = 1;
+    }
+    g.tiles_per_split = splits > 1 ? (g.n_tiles + splits - 1) / splits : (g.n_tiles > 0 ? g.n_tiles : 1);
+    g.n_splits = splits > 1 ? (g.n_tiles + g.tiles_per_split - 1) / g.tiles_per_split : 1;
+    return g;
+}
+
+}  // namespace
+
+bool attn_tc_supports(int h, int d, int kv_format) {
+    (void)h;
+    return d == kD && kv_format == SA_KV_BF16;
+}
+
+size_t attn_tc_scratch_bytes(int64_t b, int64_t s, int h, int topk) {
+    const TcGeometry g = tc_geometry(b * s, h, topk);
+    if (g.n_splits == 1) return 0;
+    const size_t ntok = (size_t)(b * s);
+    const size_t ml = align_up(ntok * g.n_splits * h * 2 * sizeof(float), 256);
+    return ml + ntok * g.n_splits * h * (size_t)kD * sizeof(float);
+}
+
+cudaError_t attn_tc_launch(const AttnCall& c) {
+    const int64_t n_tokens = c.b * c.s;
+    const TcGeometry g = tc_geometry(n_tokens, c.h, c.topk);
+    auto encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    CUtensorMap qmap;
+    const cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)(n_tokens * c.h)};
+    const cuuint64_t gstride[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult r = encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(c.q), gdim,
+                        gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+    Params p;
+    p.kv = reinterpret_cast<const __nv_bfloat16*>(c.kv);
+    p.zero_src = c.q;
+    p.sink = c.sink;
+    p.idx = c.idx;
+    p.o = reinterpret_cast<__nv_bfloat16*>(c.o);
+    p.status = c.status;
+    p.scale_log2 = c.softmax_scale * kLog2e;
+    p.s_len = c.s;
+    p.h = c.h;
+    p.hblocks = g.hblocks;
+    p.rows = c.rows;
+    p.topk = c.topk;
+    p.n_tiles = g.n_tiles;
+    p.n_splits = g.n_splits;
+    p.tiles_per_split = g.tiles_per_split;
+    p.n_tasks = n_tokens * g.hblocks * g.n_splits;
+    p.part_ml = nullptr;
+    p.part_o = nullptr;
+    if (g.n_splits > 1) {
+        const size_t ml = align_up((size_t)n_tokens * g.n_splits * c.h * 2 * sizeof(float), 256);
+        p.part_ml = reinterpret_cast<float*>(c.scratch);
+        p.part_o = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(c.scratch) + ml);
+    }
+
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) configured[dev] = true;
+    }
+    int64_t grid = sm_count();
+    if (grid > p.n_tasks) grid = p.n_tasks;
+    attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || g.n_splits == 1) return e;
+    return attn_combine_launch(p.part_ml, p.part_o, c.sink, c.o, n_tokens, c.h, kD, g.n_splits,
+                               c.stream);
+}
+
+}  // namespace sa

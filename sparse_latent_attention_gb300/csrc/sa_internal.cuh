@@ -11,6 +11,7 @@ namespace sa {
 
 // Status word bits (first 32-bit word of the workspace status block).
 constexpr uint32_t kStatusBadIndex = 1u;
+constexpr uint32_t kStatusTimeout = 2u;
 
 // Everything a sparse_attn kernel family needs for one call, already validated.
 struct AttnCall {
@@ -35,6 +36,16 @@ struct AttnCall {
 // mma.sync family (sa_attn_mma.cu)
 size_t attn_mma_scratch_bytes(int64_t b, int64_t s, int h, int d, int topk);
 cudaError_t attn_mma_launch(const AttnCall& c);
+// merge of split partials: part_ml [tokens][splits][h][2] (max in log2 units, sum),
+// part_o [tokens][splits][h][d] f32 -> o bf16 (sa_attn_mma.cu)
+cudaError_t attn_combine_launch(const float* part_ml, const float* part_o, const float* sink,
+                                void* o, int64_t n_tokens, int h, int d, int n_splits,
+                                cudaStream_t stream);
+
+// tcgen05 family (sa_attn_tc.cu)
+bool attn_tc_supports(int h, int d, int kv_format);
+size_t attn_tc_scratch_bytes(int64_t b, int64_t s, int h, int topk);
+cudaError_t attn_tc_launch(const AttnCall& c);
 
 // helpers (sa_helpers.cu)
 cudaError_t window_idxs_launch(int64_t start_pos, int64_t seqlen, int window, int32_t* idx,

@@ -262,9 +262,10 @@ def test_out_of_range_index_is_flagged_and_ignored(dev):
 
 
 @pytest.mark.parametrize("b,s,h,topk", [(2, 9, 64, 300), (4, 1, 128, 2176), (3, 1, 64, 1152)])
-def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk):
+def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk, monkeypatch):
     """Attention over e4m3 codes + e8m0 scales gives the same bits as attention over the bf16
-    round trip of the same rows (same kernel tiling and order)."""
+    round trip of the same rows (same kernel family, tiling and order)."""
+    monkeypatch.setenv("SA_FORCE_MMA", "1")
     wl = workloads.make_random(b, s, h, 512, 2500, topk, seed=300 + topk, kv_format="fp8")
     raw = _gpu.device_kv_raw(wl, dev)
     codes = torch.empty((b, wl.rows, 512), dtype=torch.uint8, device=dev)
@@ -278,3 +279,37 @@ def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk):
     o_fp8 = sa.sparse_attn(q, codes, sink, idx, wl.scale, kv_scale=scales)
     o_bf16 = sa.sparse_attn(q, rt, sink, idx, wl.scale)
     assert torch.equal(o_fp8.view(torch.int16), o_bf16.view(torch.int16))
+
+
+@pytest.mark.parametrize("case", [(2, 37, 64, 300, 200), (3, 1, 64, 5000, 1152),
+                                  (1, 9, 128, 700, 650), (2, 7, 64, 400, 130)],
+                         ids=lambda c: f"b{c[0]}s{c[1]}h{c[2]}k{c[4]}")
+def test_kernel_families_agree(dev, case, monkeypatch):
+    """The tcgen05 kernel (head_dim 512, bf16 kv) and the mma.sync kernel on the same inputs."""
+    b, s, h, rows, topk = case
+    wl = workloads.make_random(b, s, h, 512, rows, topk, seed=500 + topk, all_neg_tokens=(0,),
+                               q_scale=4.0)
+    x = _gpu.prepare(wl, dev, quantise=False)
+    o_tc = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale)
+    monkeypatch.setenv("SA_FORCE_MMA", "1")
+    o_mma = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale)
+    monkeypatch.delenv("SA_FORCE_MMA")
+    torch.cuda.synchronize()
+    assert_close_bf16(_gpu.bf16_tensor_to_u16(o_tc), _gpu.bf16_tensor_to_u16(o_mma), ATOL, RTOL,
+                      what="tc vs mma")
+
+
+@pytest.mark.parametrize("b,s,start_pos,rows,topk", [
+    (400, 1, 300, 300, 200),   # decode: every sequence's ring is rows 0..127, ~3 tasks per CTA
+    (3, 300, 0, 300, 128),     # sliding-window prefill of 3 sequences back to back
+    (2, 150, 0, 400, 200),     # window + random columns
+])
+def test_resident_rows_not_reused_across_sequences(dev, b, s, start_pos, rows, topk):
+    """Consecutive tasks on one CTA share row numbers but not data when they belong to
+    different sequences; rows kept in shared memory between tiles must match both."""
+    wl = workloads.make_random(b, s, 64, 512, rows, topk, seed=700 + b, window=128,
+                               start_pos=start_pos, neg_frac=0.05)
+    o, x, ws = _gpu_run(wl, dev, quantise=False)
+    assert sa.read_status(ws) == 0
+    want = oracle.sparse_attn(wl.q, wl.kv_raw_dense(), wl.sink, compose_idx_oracle(wl), wl.scale)
+    assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what="reuse")

@@ -26,7 +26,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    for code in range(6):
+    for code in range(7):
         assert _lib.status_string(code) not in ("", "unknown status")
     assert _lib.status_string(99) == "unknown status"
     assert _lib.version() >= 100
