@@ -9,7 +9,9 @@
 // (the full TMEM) and leaves no room for the logits.  So the gathered rows are the M dimension:
 //   S^T[128 rows x 64 heads]  = KV_tile[128 x 512] . Q^T            (4 x 8 MMAs, K = 512)
 //   O^T[512 x 64 heads]      += KV_tile^T[512 x 128] . P^T[128 x 64] (4 M-chunks x 8 MMAs)
-// TMEM holds O^T (256 columns) and two S^T buffers (2 x 64).  The same swizzled shared-memory
+// TMEM holds O^T (256 columns), two S^T buffers (2 x 64), an all-ones bf16 operand (8 columns)
+// and the softmax denominators (64 columns): l = ones . P^T is one more MMA per K step, so the
+// row sums come from the same bf16 P that multiplies V and are rescaled together with O.  The same swizzled shared-memory
 // tile is the K-major A operand of the first product and the MN-major A operand of the second.
 // The softmax runs down the columns of S^T (one TMEM lane = one gathered row per thread): the
 // column maximum is a warp max reduction plus a 4-warp exchange, and a running maximum is only
@@ -55,6 +57,8 @@ constexpr int kGroups = 4;        // 128-wide d groups (pipeline granularity)
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// TMEM columns: O^T chunks, the two S^T buffers, the all-ones operand, the row sums
+constexpr uint32_t kColO = 0, kColS = 256, kColOnes = 384, kColSum = 448;
 
 // Shared-memory map (dynamic, 1024-byte aligned base)
 constexpr uint32_t kKvBytes = kRows * kD * 2;     // 128 KB: 8 blocks of [128 rows x 128 B]
@@ -68,8 +72,8 @@ constexpr uint32_t kOffStage = kOffP + kPBytes;
 constexpr uint32_t kOffMisc = kOffStage + kStageBytes;
 
 struct Misc {
-    uint64_t q_full[kGroups], q_empty[kGroups];
-    uint64_t kv_full[kGroups], kv_empty[kGroups];
+    uint64_t q_full, q_empty;
+    uint64_t kv_full, kv_empty;
     uint64_t s_full[2], s_empty[2];
     uint64_t p_full, p_empty;
     uint64_t o_full, o_empty[kGroups];
@@ -84,13 +88,11 @@ struct Misc {
     int64_t tile_seq[2];               // sequence whose rows a tile holds (-1 = none)
     int2 copy_list[2][64];             // per producer warp: (kv row, slot) of the rows to copy
     float colred[4][kHeads];           // per-warp column max of the current tile
-    float colsum[4][kHeads];           // per-warp column sums of p of the last tile
-    float l[kHeads];                   // running sum of p (up to the last fold)
+    float suml[kHeads];                // epilogue: the task's denominators read from TMEM
     float m[kHeads];                   // running max (log2 units)
     float mu[kHeads];                  // the running max with -inf replaced by 0
     float alpha[kHeads];               // rescale factor of this tile
     float stats_m[2][kHeads];          // final max (0 when none) per task parity
-    float stats_l[2][kHeads];          // final sum per task parity
     alignas(16) float inv[2][kHeads];  // epilogue: 1 / denominator per task parity
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;  // + alignment slack
@@ -154,70 +156,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Warp reduce-scatter over 64 values per lane: afterwards lane l holds the reduction over the
-// warp of heads 2l and 2l+1 in out0 / out1.
-template <bool kMax>
-__device__ __forceinline__ void warp_reduce_scatter64(const float (&x)[64], int lane, float& out0,
-                                                      float& out1) {
-    float a[32];
-    {
-        const bool hi = lane & 16;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float send = hi ? x[i] : x[32 + i];
-            const float keep = hi ? x[32 + i] : x[i];
-            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 16);
-            a[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
-    float b[16];
-    {
-        const bool hi = lane & 8;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float send = hi ? a[i] : a[16 + i];
-            const float keep = hi ? a[16 + i] : a[i];
-            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 8);
-            b[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
-    float c[8];
-    {
-        const bool hi = lane & 4;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float send = hi ? b[i] : b[8 + i];
-            const float keep = hi ? b[8 + i] : b[i];
-            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 4);
-            c[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
-    float e[4];
-    {
-        const bool hi = lane & 2;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float send = hi ? c[i] : c[4 + i];
-            const float keep = hi ? c[4 + i] : c[i];
-            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 2);
-            e[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
-    {
-        const bool hi = lane & 1;
-        float f[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float send = hi ? e[i] : e[2 + i];
-            const float keep = hi ? e[2 + i] : e[i];
-            const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
-            f[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-        out0 = f[0];
-        out1 = f[1];
-    }
-}
-
 // Barrier among the 128 threads of one warpgroup, on an mbarrier so that it is bounded.
 __device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t& phase, volatile int* abort) {
     mbar_arrive(bar);
@@ -239,12 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &M.abort;
 
     if (tid == 0) {
-        for (int g = 0; g < kGroups; ++g) {
-            mbar_init(smem_addr(&M.q_full[g]), 1);
-            mbar_init(smem_addr(&M.q_empty[g]), 1);
-            mbar_init(smem_addr(&M.kv_full[g]), 64);
-            mbar_init(smem_addr(&M.kv_empty[g]), 1);
-        }
+        mbar_init(smem_addr(&M.q_full), 1);
+        mbar_init(smem_addr(&M.q_empty), 1);
+        mbar_init(smem_addr(&M.kv_full), 64);
+        mbar_init(smem_addr(&M.kv_empty), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&M.s_full[b]), 1);
             mbar_init(smem_addr(&M.s_empty[b]), 128);
@@ -281,6 +217,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = M.tmem_base;
+    if (warp >= 4 && warp < 8) {  // all-ones bf16 A operand for the row sums
+        tmem_st_32x32b_x8(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kColOnes, 0x3F803F80u);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     int64_t tb, te;
     task_range(p, tb, te);
 
@@ -290,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16_f32(kRows, kHeads, false, false);
             constexpr uint32_t id_o = idesc_bf16_f32(kRows, kHeads, true, true);
+            constexpr uint32_t id_l = idesc_bf16_f32(kRows, kHeads, false, true);
             // base descriptors; the per-instruction ones add a start-address offset (>> 4)
             const uint64_t a_s0 = smem_desc_sw128(s_kv, 16, 1024);
             const uint64_t b_s0 = smem_desc_sw128(s_q, 16, 1024);
@@ -302,10 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Task t = task_of(p, tau);
                 const uint32_t kp = (uint32_t)(k & 1);
                 if (t.t0 == t.t1) {  // nothing listed for this task: keep every phase in step
-                    for (int g = 0; g < kGroups && ok; ++g) {
-                        ok = mbar_wait(smem_addr(&M.q_full[g]), kp, abort);
-                        mma_commit(smem_addr(&M.q_empty[g]));
-                    }
+                    ok = mbar_wait(smem_addr(&M.q_full), kp, abort);
+                    mma_commit(smem_addr(&M.q_empty));
                     for (int c = 0; c < kGroups && ok; ++c)
                         ok = mbar_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort);
                     mma_commit(smem_addr(&M.o_full));
@@ -313,43 +255,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
                     const uint32_t b = T & 1, use = (T >> 1) & 1, tp = T & 1;
-                    const uint32_t s_col = tmem + 256 + 64 * b;
+                    const uint32_t s_col = tmem + kColS + 64 * b;
+                    // S^T = KV . Q^T: every wait first, then the 32 MMAs back to back
                     ok = mbar_wait(smem_addr(&M.s_empty[b]), use ^ 1, abort);
-                    for (int g = 0; g < kGroups && ok; ++g) {
-                        ok = mbar_wait(smem_addr(&M.kv_full[g]), tp, abort);
-                        if (ok && ti == t.t0) ok = mbar_wait(smem_addr(&M.q_full[g]), kp, abort);
-                        if (!ok) break;
-                        tc_fence_after();
-                        // K steps of 16 inside a 128-byte row advance the start address by 32 B
-                        // (2 in the descriptor's 16-byte units); the second 64-wide block of the
-                        // group is 16 KB further in the kv tile and 8 KB further in Q
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint64_t a = a_s0 + (uint64_t)(g * 2048 + (ks >> 2) * 1024 + (ks & 3) * 2);
-                            const uint64_t bq = b_s0 + (uint64_t)(g * 1024 + (ks >> 2) * 512 + (ks & 3) * 2);
-                            mma_bf16_ss(s_col, a, bq, id_s, (g | ks) != 0);
-                        }
-                        if (ti == t.t1 - 1) mma_commit(smem_addr(&M.q_empty[g]));
-                    }
+                    if (ok) ok = mbar_wait(smem_addr(&M.kv_full), tp, abort);
+                    if (ok && ti == t.t0) ok = mbar_wait(smem_addr(&M.q_full), kp, abort);
                     if (!ok) break;
+                    tc_fence_after();
+                    // K step ks (16 of 512): block ks / 4 of the tile / Q, 32 B per step inside
+                    // a 128-byte row (2 in the descriptor's 16-byte address units)
+#pragma unroll
+                    for (int ks = 0; ks < 32; ++ks)
+                        mma_bf16_ss(s_col, a_s0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                                    b_s0 + (uint64_t)((ks >> 2) * 512 + (ks & 3) * 2), id_s, ks != 0);
+                    if (ti == t.t1 - 1) mma_commit(smem_addr(&M.q_empty));
                     mma_commit(smem_addr(&M.s_full[b]));
+                    // O^T += KV^T . P^T
                     ok = mbar_wait(smem_addr(&M.p_full), tp, abort);
                     if (!ok) break;
                     tc_fence_after();
-                    for (int c = 0; c < kGroups && ok; ++c) {
+#pragma unroll
+                    for (int c = 0; c < kGroups; ++c) {
                         if (ti == t.t0) {  // the epilogue has read this chunk of the last task's O
-                            ok = mbar_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort);
-                            if (!ok) break;
+                            if (!(ok = mbar_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort))) break;
                             tc_fence_after();
                         }
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {  // 16 rows = 2 KB per K step
-                            const uint64_t a = a_o0 + (uint64_t)(c * 2048 + ks * 128);
-                            const uint64_t bp = b_o0 + (uint64_t)(ks * 128);
-                            mma_bf16_ss(tmem + 64 * c, a, bp, id_o, !(ti == t.t0 && ks == 0));
-                        }
-                        mma_commit(smem_addr(&M.kv_empty[c]));
+                        for (int ks = 0; ks < 8; ++ks)  // 16 rows = 2 KB per K step
+                            mma_bf16_ss(tmem + kColO + 64 * c, a_o0 + (uint64_t)(c * 2048 + ks * 128),
+                                        b_o0 + (uint64_t)(ks * 128), id_o, !(ti == t.t0 && ks == 0));
                     }
+                    if (!ok) break;
+                    // l += ones . P^T (every element of the A operand is 1, so one 8-column
+                    // block of TMEM serves every K step)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ts(tmem + kColSum, tmem + kColOnes, b_o0 + (uint64_t)(ks * 128),
+                                    id_l, !(ti == t.t0 && ks == 0));
+                    mma_commit(smem_addr(&M.kv_empty));
                     mma_commit(smem_addr(&M.p_empty));
                     if (ti == t.t1 - 1) mma_commit(smem_addr(&M.o_full));
                 }
@@ -367,14 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
                 const Task t = task_of(p, tau);
                 const int32_t y = (int32_t)(t.token * p.h + (int64_t)t.hb * kHeads);
-                for (int g = 0; g < kGroups && ok; ++g) {
-                    ok = mbar_wait(smem_addr(&M.q_empty[g]), (uint32_t)(k & 1) ^ 1, abort);
-                    if (!ok) break;
-                    const uint32_t bar = smem_addr(&M.q_full[g]);
-                    mbar_arrive_expect_tx(bar, 2 * 8192);
-                    tma_load_2d(s_q + (2 * g) * 8192, &q_map, 128 * g, y, bar);
-                    tma_load_2d(s_q + (2 * g + 1) * 8192, &q_map, 128 * g + 64, y, bar);
-                }
+                ok = mbar_wait(smem_addr(&M.q_empty), (uint32_t)(k & 1) ^ 1, abort);
+                if (!ok) break;
+                const uint32_t bar = smem_addr(&M.q_full);
+                mbar_arrive_expect_tx(bar, kQBytes);
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c)  // 8 boxes of [64 heads x 64 d], 128-byte swizzle
+                    tma_load_2d(s_q + c * 8192, &q_map, 64 * c, y, bar);
             }
         }
         __syncwarp();
@@ -443,11 +385,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (copy[0]) M.copy_list[pw][__popc(m0 & below)] = make_int2(jr[0], slot[0]);
                 if (copy[1]) M.copy_list[pw][n0 + __popc(m1 & below)] = make_int2(jr[1], slot[1]);
                 __syncwarp();
-                for (int g = 0; g < kGroups && ok; ++g) {
-                    ok = mbar_wait(smem_addr(&M.kv_empty[g]), tp ^ 1, abort);
+                if (ncopy <= 2) {
+                    // few new rows (e.g. the next token of a sliding window): load them into
+                    // registers now, while the previous tile is still being used, and write them
+                    // to their slots once the slots are released
+                    uint4 v[2][2];
+                    int2 ent[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        ent[e] = e < ncopy ? M.copy_list[pw][e] : make_int2(-1, 0);
+                        if (ent[e].x >= 0) {
+                            const uint4* src = reinterpret_cast<const uint4*>(kvb + (int64_t)ent[e].x * kD);
+                            v[e][0] = __ldg(src + lane);
+                            v[e][1] = __ldg(src + 32 + lane);
+                        }
+                    }
+                    ok = mbar_wait(smem_addr(&M.kv_empty), tp ^ 1, abort);
                     if (!ok) break;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (ent[e].x < 0) continue;
+                        const int r = ent[e].y;
+#pragma unroll
+                        for (int hv = 0; hv < 2; ++hv) {
+                            const int u = 32 * hv + lane;  // 16-byte unit of the 1 KB row
+                            const uint32_t dst = s_kv + (u >> 3) * 16384 + r * 128 +
+                                                 ((((u & 7) ^ (r & 7)) & 7) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                                         "r"(v[e][hv].x), "r"(v[e][hv].y), "r"(v[e][hv].z),
+                                         "r"(v[e][hv].w)
+                                         : "memory");
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(smem_addr(&M.kv_full));
+                    continue;
+                }
+                ok = mbar_wait(smem_addr(&M.kv_empty), tp ^ 1, abort);
+                if (!ok) break;
+#pragma unroll 1
+                for (int g = 0; g < kGroups; ++g) {
                     const int u = 16 * g + (lane & 15);  // 16-byte unit of the 1 KB row
-#pragma unroll 4
+#pragma unroll 1
                     for (int e = lane >> 4; e < ncopy; e += 2) {  // two rows per instruction
                         const int2 jr_s = M.copy_list[pw][e];
                         const int r = jr_s.y;
@@ -455,22 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             s_kv + (u >> 3) * 16384 + r * 128 + ((((u & 7) ^ (r & 7)) & 7) << 4);
                         cp_async16(dst, kvb + (int64_t)jr_s.x * kD + u * 8, 16u);
                     }
-                    cp_async_commit();
                 }
-                if (!ok) break;
-                // every group is in flight; publish them in order as they land
-                cp_async_wait<3>();
-                fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&M.kv_full[0]));
-                cp_async_wait<2>();
-                fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&M.kv_full[1]));
-                cp_async_wait<1>();
-                fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&M.kv_full[2]));
+                cp_async_commit();
                 cp_async_wait<0>();
                 fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&M.kv_full[3]));
+                mbar_arrive(smem_addr(&M.kv_full));
             }
         }
         cp_async_wait<0>();
@@ -491,44 +459,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
                 const uint32_t b = T & 1, use = (T >> 1) & 1, tp = T & 1;
                 const bool first = ti == t.t0;
-                ok = mbar_wait(smem_addr(&M.kv_full[0]), tp, abort);
+                ok = mbar_wait(smem_addr(&M.kv_full), tp, abort);
                 if (ok) ok = mbar_wait(smem_addr(&M.s_full[b]), use, abort);
                 if (!ok) break;
                 const bool valid = M.row_id[tp][row] >= 0;
-                const uint32_t s_addr = tmem + lane_base + 256 + 64 * b;
+                const uint32_t s_addr = tmem + lane_base + kColS + 64 * b;
                 tc_fence_after();
-                // pass 1: column maximum of the scaled logits over the 128 rows
-                {
-                    float x[64];
-                    {
-                        uint32_t r[64];
-                        tmem_ld_32x32b_x64(s_addr, r);
-                        tmem_wait_ld();
+                // pass 1: column maximum of the scaled logits over the 128 rows (two halves)
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(s_addr + 32 * half, r);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int h = 0; h < 64; ++h)
-                            x[h] = valid ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
-                    }
-#pragma unroll
-                    for (int h = 0; h < 64; ++h) {  // warp max per head, one lane stores it
+                    for (int i = 0; i < 32; ++i) {  // warp max per head, one lane stores it
+                        const float x = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
                         float mx;
-                        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(x[h]));
-                        if (lane == (h & 31)) M.colred[q4][h] = mx;
+                        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(x));
+                        if (lane == i) M.colred[q4][32 * half + i] = mx;
                     }
                 }
                 if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
                 if (row < kHeads) {
                     const int h = row;
-                    if (!first)  // fold the previous tile's column sums
-                        M.l[h] = M.alpha[h] * M.l[h] + (M.colsum[0][h] + M.colsum[1][h]) +
-                                 (M.colsum[2][h] + M.colsum[3][h]);
                     const float cm = fmaxf(fmaxf(M.colred[0][h], M.colred[1][h]),
                                            fmaxf(M.colred[2][h], M.colred[3][h]));
                     const float mo = M.m[h];
                     float mn, al = 1.f;
                     if (first) {
                         mn = cm;
-                        al = 0.f;  // the first fold starts l from this tile's sum
-                        M.l[h] = 0.f;
                     } else {
                         mn = cm > mo + kRescaleThreshold ? cm : mo;
                         if (mn != mo) {
@@ -549,9 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 if (corr) {
                     tc_fence_after();
-                    for (int c = 0; c < 2 * kGroups; ++c) {
+#pragma unroll 1
+                    for (int c = 0; c < 2 * kGroups + 2; ++c) {  // O^T (8 blocks), then l (2)
                         uint32_t r[32];
-                        const uint32_t ta = tmem + lane_base + 32 * c;  // heads 32 (c & 1) ..
+                        const uint32_t ta = tmem + lane_base +
+                                            (c < 2 * kGroups ? kColO + 32 * c : kColSum + 32 * (c & 1));
                         tmem_ld_32x32b_x32(ta, r);
                         tmem_wait_ld();
                         const float* al = &M.alpha[32 * (c & 1)];
@@ -562,53 +523,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                 }
-                // pass 2: p = 2^(x - m), the P^T row (128-byte swizzled MN-major operand)
-                float pr[64];
-                {
-                    uint32_t r[64];
-                    tmem_ld_32x32b_x64(s_addr, r);
-                    tmem_wait_ld();
+                // pass 2 (two halves): p = 2^(x - m) as the P^T row (128-byte swizzled MN-major
+                // operand), and this tile's column sums, folded in at the next tile / task end
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    float pr[32];
+                    {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(s_addr + 32 * half, r);
+                        tmem_wait_ld();
+                        const float* mu = &M.mu[32 * half];
 #pragma unroll
-                    for (int h = 0; h < 64; ++h)
-                        pr[h] = valid ? fast_exp2(__uint_as_float(r[h]) * p.scale_log2 - M.mu[h])
-                                      : 0.f;
+                        for (int i = 0; i < 32; ++i)
+                            pr[i] = valid ? fast_exp2(__uint_as_float(r[i]) * p.scale_log2 - mu[i]) : 0.f;
+                    }
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        const uint32_t u = 4 * half + u4;
+                        const uint32_t dst = s_p + row * 128 + (((u ^ (row & 7)) & 7) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                                     "r"(pack_bf16(pr[8 * u4], pr[8 * u4 + 1])),
+                                     "r"(pack_bf16(pr[8 * u4 + 2], pr[8 * u4 + 3])),
+                                     "r"(pack_bf16(pr[8 * u4 + 4], pr[8 * u4 + 5])),
+                                     "r"(pack_bf16(pr[8 * u4 + 6], pr[8 * u4 + 7])));
+                    }
                 }
                 tc_fence_before();
                 mbar_arrive(smem_addr(&M.s_empty[b]));
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint32_t dst = s_p + row * 128 + ((((uint32_t)u ^ (row & 7)) & 7) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                                 "r"(pack_bf16(pr[8 * u], pr[8 * u + 1])),
-                                 "r"(pack_bf16(pr[8 * u + 2], pr[8 * u + 3])),
-                                 "r"(pack_bf16(pr[8 * u + 4], pr[8 * u + 5])),
-                                 "r"(pack_bf16(pr[8 * u + 6], pr[8 * u + 7]))
-                                 : "memory");
-                }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(smem_addr(&M.p_full));
-                // this tile's column sums, folded in at the next tile / the end of the task
-                {
-                    float s0, s1;
-                    warp_reduce_scatter64<false>(pr, lane, s0, s1);
-                    M.colsum[q4][2 * lane] = s0;
-                    M.colsum[q4][2 * lane + 1] = s1;
-                }
             }
             if (!ok) break;
-            // final statistics of the task
+            // final statistics of the task: the running max per head (the sums are in TMEM)
             if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
             if (row < kHeads) {
-                const int h = row;
-                float l = 0.f, mh = -INFINITY;
-                if (t.t1 > t.t0) {
-                    l = M.alpha[h] * M.l[h] + (M.colsum[0][h] + M.colsum[1][h]) +
-                        (M.colsum[2][h] + M.colsum[3][h]);
-                    mh = M.m[h];
-                }
-                M.stats_l[kpar][h] = l;
-                M.stats_m[kpar][h] = mh == -INFINITY ? 0.f : mh;
+                const float mh = t.t1 > t.t0 ? M.m[row] : -INFINITY;
+                M.stats_m[kpar][row] = mh == -INFINITY ? 0.f : mh;
             }
             if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
             if (row == 0) mbar_arrive(smem_addr(&M.stats_full[kpar]));
@@ -635,9 +586,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool split = p.n_splits > 1;
             const int64_t pbase = (t.token * p.n_splits + t.split) * (int64_t)p.h + h0;
+            // the denominators: every TMEM lane of the sum block holds the same row sums
+            if (q4 < 2) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + kColSum + 32 * q4, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (lane == i) M.suml[32 * q4 + i] = t.t1 > t.t0 ? __uint_as_float(r[i]) : 0.f;
+            }
+            named_barrier(1, 128);
             if (et < kHeads) {
                 const int h = et;
-                const float l = M.stats_l[kpar][h], mu = M.stats_m[kpar][h];
+                const float l = M.suml[h], mu = M.stats_m[kpar][h];
                 float inv = 0.f;
                 if (ok && h < hc) {
                     if (split) {
@@ -650,38 +611,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 M.inv[kpar][h] = inv;
             }
             named_barrier(1, 128);
+#pragma unroll 1
             for (int c = 0; c < kGroups; ++c) {
-                uint32_t r[64];
-                tmem_ld_32x32b_x64(tmem + lane_base + 64 * c, r);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(smem_addr(&M.o_empty[c]));
                 const int dl = 32 * q4 + lane;  // d within the chunk
-                if (split) {
-                    if (ok) {
-                        float* po = p.part_o + pbase * kD + 128 * c + dl;
-#pragma unroll
-                        for (int h = 0; h < 64; ++h)
-                            if (h < hc) po[(int64_t)h * kD] = __uint_as_float(r[h]);
+#pragma unroll 1
+                for (int rh = 0; rh < 2; ++rh) {  // heads 32 rh .. 32 rh + 31
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem + lane_base + 64 * c + 32 * rh, r);
+                    tmem_wait_ld();
+                    if (rh == 1) {  // both halves of this O^T chunk are in registers
+                        tc_fence_before();
+                        mbar_arrive(smem_addr(&M.o_empty[c]));
                     }
-                    continue;
-                }
+                    if (split) {
+                        if (ok) {
+                            float* po = p.part_o + (pbase + 32 * rh) * kD + 128 * c + dl;
 #pragma unroll
-                for (int rh = 0; rh < 2; ++rh) {
-                    float iv[32];
-#pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4) {
-                        const float4 f = *reinterpret_cast<const float4*>(&M.inv[kpar][32 * rh + 4 * v4]);
-                        iv[4 * v4] = f.x;
-                        iv[4 * v4 + 1] = f.y;
-                        iv[4 * v4 + 2] = f.z;
-                        iv[4 * v4 + 3] = f.w;
+                            for (int i = 0; i < 32; ++i)
+                                if (32 * rh + i < hc) po[(int64_t)i * kD] = __uint_as_float(r[i]);
+                        }
+                        continue;
                     }
+                    const float* iv = &M.inv[kpar][32 * rh];
                     __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffStage);
 #pragma unroll
-                    for (int hl = 0; hl < 32; ++hl) {
-                        const float v = iv[hl] > 0.f ? __uint_as_float(r[32 * rh + hl]) * iv[hl] : 0.f;
-                        stage[hl * 128 + dl] = __float2bfloat16_rn(v);
+                    for (int i = 0; i < 32; ++i) {
+                        const float w = iv[i];
+                        stage[i * 128 + dl] = __float2bfloat16_rn(w > 0.f ? __uint_as_float(r[i]) * w : 0.f);
                     }
                     named_barrier(1, 128);
                     if (ok) {
