@@ -48,7 +48,7 @@ size_t sa_sparse_attn_workspace_size(int64_t b, int64_t s, int h, int d, int64_t
     if (!supported_shape(b, s, h, d, rows, topk)) return 0;
     // enough for either kernel family, whichever a call is routed to
     size_t scratch = sa::attn_mma_scratch_bytes(b, s, h, d, topk);
-    if (sa::attn_tc_supports(h, d, kv_format)) {
+    if (sa::attn_tc_supports(h, d, kv_format, b, rows)) {
         const size_t tc_scratch = sa::attn_tc_scratch_bytes(b, s, h, topk);
         if (tc_scratch > scratch) scratch = tc_scratch;
     }
@@ -101,7 +101,7 @@ sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale,
     c.scratch = reinterpret_cast<uint8_t*>(workspace) + SA_STATUS_BYTES;
     c.scratch_bytes = workspace_bytes - SA_STATUS_BYTES;
     c.stream = reinterpret_cast<cudaStream_t>(stream);
-    if (sa::attn_tc_supports(h, d, kv_format) && !force_mma())
+    if (sa::attn_tc_supports(h, d, kv_format, b, rows) && !force_mma())
         return from_cuda(sa::attn_tc_launch(c));
     return from_cuda(sa::attn_mma_launch(c));
 }

@@ -54,7 +54,11 @@ constexpr int kD = 512;           // head_dim handled by this kernel
 constexpr int kRows = 128;        // gathered rows per tile (MMA M)
 constexpr int kHeads = 64;        // heads per task (MMA N)
 constexpr int kGroups = 4;        // 128-wide d groups (pipeline granularity)
-constexpr int kThreads = 384;
+constexpr int kProdWarps = 4;                      // kv gather warps (one tile slot per thread)
+constexpr int kProdThreads = 32 * kProdWarps;
+constexpr int kWarpSoftmax = 2 + kProdWarps;        // first softmax warp
+constexpr int kWarpEpilogue = kWarpSoftmax + 4;     // first epilogue warp
+constexpr int kThreads = 32 * (kWarpEpilogue + 4);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // TMEM columns: O^T chunks, the two S^T buffers, the all-ones operand, the row sums
@@ -67,13 +71,14 @@ constexpr uint32_t kPBytes = kRows * kHeads * 2;  // 16 KB: [128 rows x 128 B]
 constexpr uint32_t kOffKv = 0;
 constexpr uint32_t kOffQ = kOffKv + kKvBytes;
 constexpr uint32_t kOffP = kOffQ + kQBytes;
-constexpr uint32_t kStageBytes = 32 * kRows * 2;  // 8 KB: o staging [32 heads x 128 d]
+// o staging: [32 heads x 64 d] boxes of 128-byte rows, 128-byte swizzle, one per 64 d of a chunk
+constexpr uint32_t kStageBoxBytes = 32 * 128;
 constexpr uint32_t kOffStage = kOffP + kPBytes;
-constexpr uint32_t kOffMisc = kOffStage + kStageBytes;
+constexpr uint32_t kOffMisc = kOffStage + 2 * kStageBoxBytes;
 
 struct Misc {
     uint64_t q_full, q_empty;
-    uint64_t kv_full, kv_empty;
+    uint64_t kv_full[kGroups], kv_empty[kGroups];  // per 128-d chunk of the kv tile
     uint64_t s_full[2], s_empty[2];
     uint64_t p_full, p_empty;
     uint64_t o_full, o_empty[kGroups];
@@ -86,7 +91,7 @@ struct Misc {
     uint32_t ring_bits[2][4];          // residues mod 128 of a tile's valid rows
     int ring_count[2];                 // number of valid rows of a tile
     int64_t tile_seq[2];               // sequence whose rows a tile holds (-1 = none)
-    int2 copy_list[2][64];             // per producer warp: (kv row, slot) of the rows to copy
+    int2 copy_list[kProdWarps][32];    // per producer warp: (kv row, slot) of the rows to copy
     float colred[4][kHeads];           // per-warp column max of the current tile
     float suml[kHeads];                // epilogue: the task's denominators read from TMEM
     float m[kHeads];                   // running max (log2 units)
@@ -94,13 +99,13 @@ struct Misc {
     float alpha[kHeads];               // rescale factor of this tile
     float stats_m[2][kHeads];          // final max (0 when none) per task parity
     alignas(16) float inv[2][kHeads];  // epilogue: 1 / denominator per task parity
+    float sink[128];                   // the sinks of every head
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
     const __nv_bfloat16* kv;
-    const void* zero_src;  // any valid 16-byte aligned address: source of zero-byte copies
     const float* sink;
     const int32_t* idx;
     __nv_bfloat16* o;
@@ -120,7 +125,7 @@ struct Params {
 };
 
 struct Task {
-    int64_t token;
+    int64_t token, seq, pos;  // query token (flat), its sequence and position in it
     int hb, split, t0, t1;
 };
 
@@ -139,16 +144,42 @@ __device__ __forceinline__ Task task_of(const Params& p, int64_t tau) {
     const int64_t th = tau / p.n_splits;
     t.hb = (int)(th % p.hblocks);
     t.token = th / p.hblocks;
+    t.seq = t.token / p.s_len;
+    t.pos = t.token - t.seq * p.s_len;
     t.t0 = t.split * p.tiles_per_split;
     t.t1 = min(p.n_tiles, t.t0 + p.tiles_per_split);
     if (t.t1 < t.t0) t.t1 = t.t0;
     return t;
 }
 
+// The task after t (splits fastest, then head blocks, then tokens), without divisions.
+__device__ __forceinline__ void task_step(const Params& p, Task& t) {
+    if (++t.split == p.n_splits) {
+        t.split = 0;
+        if (++t.hb == p.hblocks) {
+            t.hb = 0;
+            ++t.token;
+            if (++t.pos == p.s_len) {
+                t.pos = 0;
+                ++t.seq;
+            }
+        }
+    }
+    t.t0 = t.split * p.tiles_per_split;
+    t.t1 = min(p.n_tiles, t.t0 + p.tiles_per_split);
+    if (t.t1 < t.t0) t.t1 = t.t0;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// A 4-byte shared-memory store in asm without a memory clobber: the compiler may move the
+// surrounding shared-memory reads across it (they never touch the same bytes).
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -165,7 +196,8 @@ __device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t& phase, volatile 
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap q_map, Params p) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap o_map,
+                   Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -179,8 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         mbar_init(smem_addr(&M.q_full), 1);
         mbar_init(smem_addr(&M.q_empty), 1);
-        mbar_init(smem_addr(&M.kv_full), 64);
-        mbar_init(smem_addr(&M.kv_empty), 1);
+        for (int c = 0; c < kGroups; ++c) {
+            mbar_init(smem_addr(&M.kv_full[c]), kProdThreads);
+            mbar_init(smem_addr(&M.kv_empty[c]), 1);
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&M.s_full[b]), 1);
             mbar_init(smem_addr(&M.s_empty[b]), 128);
@@ -192,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kGroups; ++c) mbar_init(smem_addr(&M.o_empty[c]), 128);
         mbar_init(smem_addr(&M.sm_bar), 128);
         mbar_init(smem_addr(&M.ep_bar), 128);
-        mbar_init(smem_addr(&M.pr_bar), 64);
+        mbar_init(smem_addr(&M.pr_bar), kProdThreads);
         mbar_init(smem_addr(&M.done), 1);
         M.abort = 0;
         M.need_corr[0] = M.need_corr[1] = 0;
@@ -209,15 +243,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         M.ring_count[tid] = 0;
         M.tile_seq[tid] = -1;
     }
+    for (int i = tid; i < p.h; i += kThreads) M.sink[i] = p.sink[i];
     for (uint32_t i = tid; i < kKvBytes / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + kOffKv)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1 && lane == 0) tma_prefetch_desc(&q_map);
+    if (warp == kWarpEpilogue && lane == 0) tma_prefetch_desc(&o_map);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = M.tmem_base;
-    if (warp >= 4 && warp < 8) {  // all-ones bf16 A operand for the row sums
+    if (warp >= kWarpSoftmax && warp < kWarpEpilogue) {  // all-ones bf16 A operand for the row sums
         tmem_st_32x32b_x8(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kColOnes, 0x3F803F80u);
         tmem_wait_st();
     }
@@ -242,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t T = 0;
             int64_t k = 0;
             bool ok = true;
-            for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
-                const Task t = task_of(p, tau);
+            Task t = task_of(p, tb);
+            for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
                 const uint32_t kp = (uint32_t)(k & 1);
                 if (t.t0 == t.t1) {  // nothing listed for this task: keep every phase in step
                     ok = mbar_wait(smem_addr(&M.q_full), kp, abort);
@@ -258,16 +294,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t s_col = tmem + kColS + 64 * b;
                     // S^T = KV . Q^T: every wait first, then the 32 MMAs back to back
                     ok = mbar_wait(smem_addr(&M.s_empty[b]), use ^ 1, abort);
-                    if (ok) ok = mbar_wait(smem_addr(&M.kv_full), tp, abort);
                     if (ok && ti == t.t0) ok = mbar_wait(smem_addr(&M.q_full), kp, abort);
                     if (!ok) break;
-                    tc_fence_after();
                     // K step ks (16 of 512): block ks / 4 of the tile / Q, 32 B per step inside
-                    // a 128-byte row (2 in the descriptor's 16-byte address units)
+                    // a 128-byte row (2 in the descriptor's 16-byte address units); each 128-d
+                    // chunk of the tile as soon as it has landed
 #pragma unroll
-                    for (int ks = 0; ks < 32; ++ks)
-                        mma_bf16_ss(s_col, a_s0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
-                                    b_s0 + (uint64_t)((ks >> 2) * 512 + (ks & 3) * 2), id_s, ks != 0);
+                    for (int c = 0; c < kGroups; ++c) {
+                        if (!(ok = mbar_wait(smem_addr(&M.kv_full[c]), tp, abort))) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int ks = 8 * c; ks < 8 * c + 8; ++ks)
+                            mma_bf16_ss(s_col, a_s0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                                        b_s0 + (uint64_t)((ks >> 2) * 512 + (ks & 3) * 2), id_s,
+                                        ks != 0);
+                    }
+                    if (!ok) break;
                     if (ti == t.t1 - 1) mma_commit(smem_addr(&M.q_empty));
                     mma_commit(smem_addr(&M.s_full[b]));
                     // O^T += KV^T . P^T
@@ -284,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int ks = 0; ks < 8; ++ks)  // 16 rows = 2 KB per K step
                             mma_bf16_ss(tmem + kColO + 64 * c, a_o0 + (uint64_t)(c * 2048 + ks * 128),
                                         b_o0 + (uint64_t)(ks * 128), id_o, !(ti == t.t0 && ks == 0));
+                        mma_commit(smem_addr(&M.kv_empty[c]));  // chunk c of the tile is read
                     }
                     if (!ok) break;
                     // l += ones . P^T (every element of the A operand is 1, so one 8-column
@@ -292,7 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < 8; ++ks)
                         mma_bf16_ts(tmem + kColSum, tmem + kColOnes, b_o0 + (uint64_t)(ks * 128),
                                     id_l, !(ti == t.t0 && ks == 0));
-                    mma_commit(smem_addr(&M.kv_empty));
                     mma_commit(smem_addr(&M.p_empty));
                     if (ti == t.t1 - 1) mma_commit(smem_addr(&M.o_full));
                 }
@@ -307,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int64_t k = 0;
             bool ok = true;
-            for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
-                const Task t = task_of(p, tau);
+            Task t = task_of(p, tb);
+            for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
                 const int32_t y = (int32_t)(t.token * p.h + (int64_t)t.hb * kHeads);
                 ok = mbar_wait(smem_addr(&M.q_empty), (uint32_t)(k & 1) ^ 1, abort);
                 if (!ok) break;
@@ -318,44 +360,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 8; ++c)  // 8 boxes of [64 heads x 64 d], 128-byte swizzle
                     tma_load_2d(s_q + c * 8192, &q_map, 64 * c, y, bar);
             }
+            // after a failed wait, let the last Q load land before the CTA exits
+            if (!ok && k > 0) mbar_drain(smem_addr(&M.q_full), (uint32_t)((k - 1) & 1));
         }
         __syncwarp();
-    } else if (warp < 4) {
+    } else if (warp < kWarpSoftmax) {
         // ------------------------------------------------------------------ kv gather
-        const int pw = warp - 2;       // producer warp 0 / 1
-        const int pt_id = tid - 64;    // 0 .. 63
+        // Each thread resolves one of the tile's 128 slots; every warp lists the rows it copies
+        // and copies each 128-d chunk of them (cp.async, one commit group per chunk) as soon as
+        // the previous tile's P.V has finished reading that chunk; chunk c is signalled once the
+        // group has landed.
+        const int pw = warp - 2;       // producer warp 0 .. kProdWarps - 1
+        const int pt_id = tid - 64;    // the tile slot (column placement) this thread resolves
         uint32_t T = 0, pr_phase = 0;
         bool ok = true;
-        for (int64_t tau = tb; tau < te && ok; ++tau) {
-            const Task t = task_of(p, tau);
-            const int64_t bi = t.token / p.s_len;
+        Task t = task_of(p, tb);
+        for (int64_t tau = tb; tau < te && ok; ++tau, task_step(p, t)) {
+            const int64_t bi = t.seq;
             const int32_t* idx_tok = p.idx + t.token * (int64_t)p.topk;
             const __nv_bfloat16* kvb = p.kv + bi * p.rows * (int64_t)kD;
             for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
                 const uint32_t tp = T & 1;
-                // the two tile rows this thread resolves: r = pt_id and pt_id + 64
-                int jr[2];
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int col = ti * kRows + pt_id + 64 * hf;
-                    int j = col < p.topk ? __ldg(idx_tok + col) : -1;
-                    if (j < -1 || j >= p.rows) {
-                        atomicOr(p.status, kStatusBadIndex);
-                        j = -1;
-                    }
-                    jr[hf] = j;
+                const int col = ti * kRows + pt_id;
+                int j = col < p.topk ? __ldg(idx_tok + col) : -1;
+                if (j < -1 || j >= p.rows) {
+                    atomicOr(p.status, kStatusBadIndex);
+                    j = -1;
                 }
-                // placement: ring (slot = j mod 128) when the valid rows' residues are distinct
-                M.row_id[tp][pt_id] = -1;
-                M.row_id[tp][pt_id + 64] = -1;
-                int nvalid = 0;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                    if (jr[hf] >= 0) {
-                        atomicOr(&M.ring_bits[tp][(jr[hf] & 127) >> 5], 1u << (jr[hf] & 31));
-                        ++nvalid;
-                    }
-                if (nvalid) atomicAdd(&M.ring_count[tp], nvalid);
+                // placement: ring (slot = j mod 128) when the valid rows' residues are distinct.
+                // (row_id[tp] is only written after the tile barrier below: the softmax of the
+                // tile two back, which has the same parity, may still be reading it until then.)
+                if (j >= 0) {
+                    atomicOr(&M.ring_bits[tp][(j & 127) >> 5], 1u << (j & 31));
+                    atomicAdd(&M.ring_count[tp], 1);
+                }
                 if (pt_id == 0) M.tile_seq[tp] = bi;
                 if (!(ok = wg_sync(smem_addr(&M.pr_bar), pr_phase, abort))) break;
                 // a slot's row can be kept only if it belongs to this same sequence
@@ -363,32 +401,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool ring = __popc(M.ring_bits[tp][0]) + __popc(M.ring_bits[tp][1]) +
                                       __popc(M.ring_bits[tp][2]) + __popc(M.ring_bits[tp][3]) ==
                                   M.ring_count[tp];
-                int slot[2];
-                bool copy[2];
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int j = jr[hf];
-                    slot[hf] = ring ? (j & 127) : pt_id + 64 * hf;
-                    copy[hf] = j >= 0 && (!same_seq || M.row_id[tp ^ 1][slot[hf]] != j);
-                    if (j >= 0) M.row_id[tp][slot[hf]] = j;
-                }
+                // this thread's own slot is empty unless a row claims it
+                const bool claimed = ring ? ((M.ring_bits[tp][pt_id >> 5] >> (pt_id & 31)) & 1) != 0
+                                          : j >= 0;
+                if (!claimed) M.row_id[tp][pt_id] = -1;
+                const int slot = ring ? (j & 127) : pt_id;
+                const bool copy = j >= 0 && (!same_seq || M.row_id[tp ^ 1][slot] != j);
+                if (j >= 0) M.row_id[tp][slot] = j;
                 if (pt_id == 0) {  // the next tile (other parity) starts from a clean slate
                     M.ring_bits[tp ^ 1][0] = M.ring_bits[tp ^ 1][1] = 0;
                     M.ring_bits[tp ^ 1][2] = M.ring_bits[tp ^ 1][3] = 0;
                     M.ring_count[tp ^ 1] = 0;
                 }
-                // the rows this warp copies, compacted into a list (ballot prefix counts)
-                const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, copy[0]);
-                const uint32_t m1 = __ballot_sync(0xFFFFFFFFu, copy[1]);
-                const uint32_t below = (1u << lane) - 1u;
-                const int n0 = __popc(m0), ncopy = n0 + __popc(m1);
-                if (copy[0]) M.copy_list[pw][__popc(m0 & below)] = make_int2(jr[0], slot[0]);
-                if (copy[1]) M.copy_list[pw][n0 + __popc(m1 & below)] = make_int2(jr[1], slot[1]);
+                // the rows this warp copies, compacted into a list (ballot prefix count)
+                const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, copy);
+                const int ncopy = __popc(m0);
+                if (copy) M.copy_list[pw][__popc(m0 & ((1u << lane) - 1u))] = make_int2(j, slot);
                 __syncwarp();
                 if (ncopy <= 2) {
                     // few new rows (e.g. the next token of a sliding window): load them into
                     // registers now, while the previous tile is still being used, and write them
-                    // to their slots once the slots are released
+                    // to their slots once the whole tile is released
                     uint4 v[2][2];
                     int2 ent[2];
 #pragma unroll
@@ -400,7 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v[e][1] = __ldg(src + 32 + lane);
                         }
                     }
-                    ok = mbar_wait(smem_addr(&M.kv_empty), tp ^ 1, abort);
+#pragma unroll 1
+                    for (int c = 0; c < kGroups && ok; ++c)
+                        ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
                     if (!ok) break;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -418,31 +453,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     fence_proxy_async_smem();
-                    mbar_arrive(smem_addr(&M.kv_full));
+#pragma unroll
+                    for (int c = 0; c < kGroups; ++c) mbar_arrive(smem_addr(&M.kv_full[c]));
                     continue;
                 }
-                ok = mbar_wait(smem_addr(&M.kv_empty), tp ^ 1, abort);
-                if (!ok) break;
-#pragma unroll 1
-                for (int g = 0; g < kGroups; ++g) {
-                    const int u = 16 * g + (lane & 15);  // 16-byte unit of the 1 KB row
-#pragma unroll 1
-                    for (int e = lane >> 4; e < ncopy; e += 2) {  // two rows per instruction
-                        const int2 jr_s = M.copy_list[pw][e];
-                        const int r = jr_s.y;
-                        const uint32_t dst =
-                            s_kv + (u >> 3) * 16384 + r * 128 + ((((u & 7) ^ (r & 7)) & 7) << 4);
-                        cp_async16(dst, kvb + (int64_t)jr_s.x * kD + u * 8, 16u);
-                    }
+                // this lane's rows of the list: entries lane / 16 + 2 i (two rows per instruction)
+                int2 ent[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int e = (lane >> 4) + 2 * i;
+                    ent[i] = e < ncopy ? M.copy_list[pw][e] : make_int2(-1, 0);
                 }
-                cp_async_commit();
+                // chunk c = 16-byte units 16 c .. 16 c + 15 of each row (blocks 2 c and 2 c + 1)
+#pragma unroll
+                for (int c = 0; c < kGroups; ++c) {
+                    if (ok) ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
+                    if (ok) {
+                        const int u = 16 * c + (lane & 15);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (ent[i].x < 0) break;
+                            const int r = ent[i].y;
+                            const uint32_t dst =
+                                s_kv + (u >> 3) * 16384 + r * 128 + ((((u & 7) ^ (r & 7)) & 7) << 4);
+                            cp_async16(dst, kvb + (int64_t)ent[i].x * kD + u * 8, 16u);
+                        }
+                    }
+                    cp_async_commit();  // (an empty group after a failed wait keeps the count)
+                }
+                if (!ok) break;
+                cp_async_wait<3>();
+                fence_proxy_async_smem();
+                mbar_arrive(smem_addr(&M.kv_full[0]));
+                cp_async_wait<2>();
+                fence_proxy_async_smem();
+                mbar_arrive(smem_addr(&M.kv_full[1]));
+                cp_async_wait<1>();
+                fence_proxy_async_smem();
+                mbar_arrive(smem_addr(&M.kv_full[2]));
                 cp_async_wait<0>();
                 fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&M.kv_full));
+                mbar_arrive(smem_addr(&M.kv_full[3]));
             }
         }
         cp_async_wait<0>();
-    } else if (warp < 8) {
+    } else if (warp < kWarpEpilogue) {
         // ------------------------------------------------------------------ softmax
         // Per tile: column max of the logits -> running max m (raised only past the threshold),
         // p = 2^(x - m) written as P^T, and the tile's column sums; the sums are folded into the
@@ -453,13 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t T = 0, sm_phase = 0;
         int64_t k = 0;
         bool ok = true;
-        for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
-            const Task t = task_of(p, tau);
+        Task t = task_of(p, tb);
+        for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
             const int kpar = (int)(k & 1);
             for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
                 const uint32_t b = T & 1, use = (T >> 1) & 1, tp = T & 1;
                 const bool first = ti == t.t0;
-                ok = mbar_wait(smem_addr(&M.kv_full), tp, abort);
+                ok = mbar_wait(smem_addr(&M.kv_full[0]), tp, abort);  // the tile's row ids
                 if (ok) ok = mbar_wait(smem_addr(&M.s_full[b]), use, abort);
                 if (!ok) break;
                 const bool valid = M.row_id[tp][row] >= 0;
@@ -566,18 +621,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue
-        // O^T chunk c (128 d x 64 heads) leaves TMEM at once (the MMA may refill it); the bf16
-        // values go through a [32 heads x 128 d] shared-memory stage so that o is written as
-        // 256-byte runs with 16-byte stores.  Every thread passes every barrier of a task, even
-        // after a failed wait, so the warpgroup's barriers never split.
+        // O^T chunk c (128 d x 64 heads) leaves TMEM at once (the MMA may refill it), is scaled by
+        // 1 / denominator, packed to bf16 and transposed through a swizzled shared-memory stage
+        // that TMA stores to o (one [32 heads x 64 d] box per 64 d).  Every thread passes every
+        // barrier of a task, even after a failed wait, so the warpgroup's barriers never split.
         const int q4 = warp & 3;
-        const int et = tid - 256;
+        const int et = tid - 32 * kWarpEpilogue;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        // stage address of this thread's d pair: box q4 / 2, 16-byte unit st_unit of the
+        // 128-byte row (before the swizzle), byte 4 (k & 3) inside it
         const uint32_t s_stage = smem_addr(smem + kOffStage);
+        const int odd = lane & 1;
+        const uint32_t sel = odd ? 0x3276u : 0x5410u;
+        const uint32_t st_unit = 4 * (q4 & 1) + (lane >> 3);
+        const uint32_t st_base = s_stage + (q4 >> 1) * kStageBoxBytes + 4 * ((lane >> 1) & 3);
         int64_t k = 0;
         bool ok = true;
-        for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
-            const Task t = task_of(p, tau);
+        Task t = task_of(p, tb);
+        for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
             const int kpar = (int)(k & 1);
             const int h0 = t.hb * kHeads;
             const int hc = min(kHeads, p.h - h0);
@@ -605,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.part_ml[(pbase + h) * 2 + 0] = mu;
                         p.part_ml[(pbase + h) * 2 + 1] = l;
                     } else if (l > 0.f) {
-                        inv = 1.f / (l + fast_exp2(p.sink[h0 + h] * kLog2e - mu));
+                        inv = 1.f / (l + fast_exp2(M.sink[h0 + h] * kLog2e - mu));
                     }
                 }
                 M.inv[kpar][h] = inv;
@@ -613,52 +674,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_barrier(1, 128);
 #pragma unroll 1
             for (int c = 0; c < kGroups; ++c) {
-                const int dl = 32 * q4 + lane;  // d within the chunk
-#pragma unroll 1
-                for (int rh = 0; rh < 2; ++rh) {  // heads 32 rh .. 32 rh + 31
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + 64 * c + 32 * rh, r);
-                    tmem_wait_ld();
-                    if (rh == 1) {  // both halves of this O^T chunk are in registers
-                        tc_fence_before();
-                        mbar_arrive(smem_addr(&M.o_empty[c]));
-                    }
-                    if (split) {
-                        if (ok) {
-                            float* po = p.part_o + (pbase + 32 * rh) * kD + 128 * c + dl;
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (32 * rh + i < hc) po[(int64_t)i * kD] = __uint_as_float(r[i]);
-                        }
-                        continue;
-                    }
-                    const float* iv = &M.inv[kpar][32 * rh];
-                    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffStage);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float w = iv[i];
-                        stage[i * 128 + dl] = __float2bfloat16_rn(w > 0.f ? __uint_as_float(r[i]) * w : 0.f);
-                    }
-                    named_barrier(1, 128);
+                uint32_t r[kHeads];
+                tmem_ld_32x32b_x64(tmem + lane_base + 64 * c, r);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(smem_addr(&M.o_empty[c]));  // the MMA may refill this chunk now
+                if (split) {
                     if (ok) {
+                        float* po = p.part_o + pbase * kD + 128 * c + 32 * q4 + lane;
 #pragma unroll
-                        for (int it = 0; it < 4; ++it) {
-                            const int hl = 8 * q4 + 2 * it + (lane >> 4);
-                            const int h = 32 * rh + hl;
-                            if (h < hc) {
-                                uint4 v;
-                                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                                             : "r"(s_stage + hl * 256 + (lane & 15) * 16));
-                                *reinterpret_cast<uint4*>(p.o + (t.token * p.h + h0 + h) * (int64_t)kD +
-                                                          128 * c + (lane & 15) * 8) = v;
-                            }
+                        for (int i = 0; i < kHeads; ++i)
+                            if (i < hc) po[(int64_t)i * kD] = __uint_as_float(r[i]);
+                    }
+                    continue;
+                }
+#pragma unroll
+                for (int rh = 0; rh < 2; ++rh) {  // heads 32 rh .. 32 rh + 31 of the block
+                    // Lanes 2k and 2k+1 hold d = 2k and 2k+1 of every head.  Two heads a and
+                    // a + 4 are packed per word, the neighbours swap words, and the even lane
+                    // keeps head a's (d, d+1) pair, the odd lane head a + 4's.  Rows a and a + 4
+                    // of the swizzled box sit in opposite 64-byte halves of the banks.
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const float4 wa = *reinterpret_cast<const float4*>(&M.inv[kpar][32 * rh + 8 * m]);
+                        const float4 wb = *reinterpret_cast<const float4*>(&M.inv[kpar][32 * rh + 8 * m + 4]);
+                        const float fa[4] = {wa.x, wa.y, wa.z, wa.w}, fb[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int a = 32 * rh + 8 * m + i;
+                            const float va = fa[i] > 0.f ? __uint_as_float(r[a]) * fa[i] : 0.f;
+                            const float vb = fb[i] > 0.f ? __uint_as_float(r[a + 4]) * fb[i] : 0.f;
+                            const uint32_t pk = pack_bf16(va, vb);
+                            const uint32_t x = __shfl_xor_sync(0xffffffffu, pk, 1);
+                            const uint32_t row = 8 * m + i + 4 * odd;
+                            st_shared_b32(st_base + row * 128 + (((st_unit ^ row) & 7) << 4),
+                                          __byte_perm(pk, x, sel));
                         }
+                    }
+                    fence_proxy_async_smem();
+                    named_barrier(1, 128);
+                    if (et == 0) {
+                        if (ok && h0 + 32 * rh < p.h) {
+                            const int32_t y = h0 + 32 * rh, z = (int32_t)t.token;
+                            tma_store_3d(&o_map, s_stage, 128 * c, y, z);
+                            tma_store_3d(&o_map, s_stage + kStageBoxBytes, 128 * c + 64, y, z);
+                            bulk_commit();
+                        }
+                        bulk_wait_read_all();  // the stage may be rewritten
                     }
                     named_barrier(1, 128);
                 }
             }
         }
+        if (et == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -724,8 +792,10 @@ TcGeometry tc_geometry(int64_t n_tokens, int h, int topk) {
 
 }  // namespace
 
-bool attn_tc_supports(int h, int d, int kv_format) {
+bool attn_tc_supports(int h, int d, int kv_format, int64_t b, int64_t rows) {
     (void)h;
+    (void)b;
+    (void)rows;
     return d == kD && kv_format == SA_KV_BF16;
 }
 
@@ -752,10 +822,19 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // o as [tokens][h][512]: a [1 x 32 x 64] box is clipped at h for a partial head block
+    CUtensorMap omap;
+    const cuuint64_t odim[3] = {(cuuint64_t)kD, (cuuint64_t)c.h, (cuuint64_t)n_tokens};
+    const cuuint64_t ostride[2] = {(cuuint64_t)kD * 2, (cuuint64_t)c.h * kD * 2};
+    const cuuint32_t obox[3] = {64, (cuuint32_t)(c.h < 32 ? c.h : 32), 1};
+    const cuuint32_t oestride[3] = {1, 1, 1};
+    r = encode(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c.o, odim, ostride, obox, oestride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
     Params p;
     p.kv = reinterpret_cast<const __nv_bfloat16*>(c.kv);
-    p.zero_src = c.q;
     p.sink = c.sink;
     p.idx = c.idx;
     p.o = reinterpret_cast<__nv_bfloat16*>(c.o);
@@ -790,7 +869,7 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
     }
     int64_t grid = sm_count();
     if (grid > p.n_tasks) grid = p.n_tasks;
-    attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, p);
+    attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || g.n_splits == 1) return e;
     return attn_combine_launch(p.part_ml, p.part_o, c.sink, c.o, n_tokens, c.h, kD, g.n_splits,

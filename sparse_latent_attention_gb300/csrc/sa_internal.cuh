@@ -43,7 +43,8 @@ cudaError_t attn_combine_launch(const float* part_ml, const float* part_o, const
                                 cudaStream_t stream);
 
 // tcgen05 family (sa_attn_tc.cu)
-bool attn_tc_supports(int h, int d, int kv_format);
+// d = 512 with bf16 kv
+bool attn_tc_supports(int h, int d, int kv_format, int64_t b, int64_t rows);
 size_t attn_tc_scratch_bytes(int64_t b, int64_t s, int h, int topk);
 cudaError_t attn_tc_launch(const AttnCall& c);
 

@@ -71,6 +71,16 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
     return false;
 }
 
+// After a failed wait elsewhere: wait (bounded, ignoring the abort flag) for the phase of
+// `parity` that this thread's own asynchronous copies complete, so that none is still writing
+// shared memory when the CTA exits.
+__device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < (1u << 20); ++i) {
+        if (mbar_try_wait(bar, parity)) return;
+        __nanosleep(256);
+    }
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
     if (mbar_test_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, abort);
@@ -124,6 +134,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         "l"(tmap), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+
+// Tiled 3-D store of a shared-memory box to global memory (bulk async-group completion).  The
+// box is clipped at the tensor's extents; the start coordinates must not be negative.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t x, int32_t y,
+                                             int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            tmap),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed bulk store has finished reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed bulk store has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
