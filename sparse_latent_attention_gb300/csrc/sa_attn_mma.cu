@@ -372,38 +372,45 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(Params p) {
 
 // Merge the split partials of one token: M = max_s m_s;
 // o = sum_s 2^(m_s - M) O_s / (2^(sink log2e - M) + sum_s 2^(m_s - M) l_s), zero when no row.
+// One block of d / 4 threads per (token, head): thread i merges columns 4 i .. 4 i + 3 of the
+// split partials.  (The few split statistics every thread reads stay in L1.)
 __global__ void attn_combine_kernel(const float* __restrict__ part_ml,
                                     const float* __restrict__ part_o,
                                     const float* __restrict__ sink, __nv_bfloat16* __restrict__ o,
                                     int h, int d, int n_splits) {
-    const int64_t token = blockIdx.x;
-    for (int hh = threadIdx.y; hh < h; hh += blockDim.y) {
-        float M = -INFINITY, L = 0.f;
-        for (int sp = 0; sp < n_splits; ++sp) {
-            const float* ml = part_ml + ((token * n_splits + sp) * h + hh) * 2;
-            if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
-        }
-        const float Mu = M == -INFINITY ? 0.f : M;
-        for (int sp = 0; sp < n_splits; ++sp) {
-            const float* ml = part_ml + ((token * n_splits + sp) * h + hh) * 2;
-            if (ml[1] > 0.f) L += ml[1] * fast_exp2(ml[0] - Mu);
-        }
-        const float inv = L > 0.f ? 1.f / (L + fast_exp2(sink[hh] * kLog2e - Mu)) : 0.f;
-        for (int c = threadIdx.x * 2; c < d; c += blockDim.x * 2) {
-            float a = 0.f, b = 0.f;
-            for (int sp = 0; sp < n_splits; ++sp) {
-                const float* ml = part_ml + ((token * n_splits + sp) * h + hh) * 2;
-                if (!(ml[1] > 0.f)) continue;
-                const float w = fast_exp2(ml[0] - Mu);
-                const float2 v = *reinterpret_cast<const float2*>(
-                    part_o + ((token * n_splits + sp) * h + hh) * (int64_t)d + c);
-                a += w * v.x;
-                b += w * v.y;
-            }
-            *reinterpret_cast<uint32_t*>(o + (token * h + hh) * (int64_t)d + c) =
-                pack_bf16(a * inv, b * inv);
-        }
+    const int64_t th = blockIdx.x;  // token * h + head
+    const int hh = (int)(th % h);
+    const int64_t token = th / h;
+    const int c = 4 * threadIdx.x;
+    const float* ml0 = part_ml + (token * n_splits * (int64_t)h + hh) * 2;  // split 0
+    const int64_t ml_step = (int64_t)h * 2;                                  // next split
+    float M = -INFINITY, L = 0.f;
+    for (int sp = 0; sp < n_splits; ++sp) {
+        const float* ml = ml0 + sp * ml_step;
+        if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
     }
+    const float Mu = M == -INFINITY ? 0.f : M;
+    for (int sp = 0; sp < n_splits; ++sp) {
+        const float* ml = ml0 + sp * ml_step;
+        if (ml[1] > 0.f) L += ml[1] * fast_exp2(ml[0] - Mu);
+    }
+    const float inv = L > 0.f ? 1.f / (L + fast_exp2(sink[hh] * kLog2e - Mu)) : 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < n_splits; ++sp) {
+        const float* ml = ml0 + sp * ml_step;
+        if (!(ml[1] > 0.f)) continue;
+        const float w = fast_exp2(ml[0] - Mu);
+        const float4 v = *reinterpret_cast<const float4*>(
+            part_o + ((token * n_splits + sp) * h + hh) * (int64_t)d + c);
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+    }
+    uint2 out;
+    out.x = pack_bf16(acc.x * inv, acc.y * inv);
+    out.y = pack_bf16(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(o + th * (int64_t)d + c) = out;
 }
 
 struct Geometry {
@@ -509,7 +516,8 @@ cudaError_t attn_mma_launch(const AttnCall& c) {
 cudaError_t attn_combine_launch(const float* part_ml, const float* part_o, const float* sink,
                                 void* o, int64_t n_tokens, int h, int d, int n_splits,
                                 cudaStream_t stream) {
-    attn_combine_kernel<<<(unsigned)n_tokens, dim3(32, 8), 0, stream>>>(
+    if (n_tokens * h == 0) return cudaSuccess;
+    attn_combine_kernel<<<(unsigned)(n_tokens * h), d / 4, 0, stream>>>(
         part_ml, part_o, sink, reinterpret_cast<__nv_bfloat16*>(o), h, d, n_splits);
     return cudaGetLastError();
 }
