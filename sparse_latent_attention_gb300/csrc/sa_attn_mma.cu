@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sa_fp8.cuh"
 #include "sa_internal.cuh"
 
 namespace sa {
@@ -96,30 +97,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 2^(e - 127) for an e8m0 byte (e = 0 is 2^-127, a subnormal f32).
-__device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
-    return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
-}
-
-// Sixteen e4m3 codes times one power-of-two scale -> sixteen bf16 values (exact).
-__device__ __forceinline__ void dequant16(uint4 c, float sc, uint4& lo, uint4& hi) {
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-    uint32_t out[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint16_t pair = (uint16_t)(w[i] >> (16 * half));
-            uint32_t h2;
-            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
-            const float a = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * sc;
-            const float b = __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * sc;
-            out[2 * i + half] = pack_bf16(a, b);
-        }
-    }
-    lo = make_uint4(out[0], out[1], out[2], out[3]);
-    hi = make_uint4(out[4], out[5], out[6], out[7]);
-}
+using fp8::dequant16;
+using fp8::e8m0_to_f32;
 
 template <int D, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(Params p) {

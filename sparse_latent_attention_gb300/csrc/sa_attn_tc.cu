@@ -42,6 +42,7 @@
 
 #include <mutex>
 
+#include "sa_fp8.cuh"
 #include "sa_internal.cuh"
 #include "sa_tc.cuh"
 
@@ -100,12 +101,15 @@ struct Misc {
     float stats_m[2][kHeads];          // final max (0 when none) per task parity
     alignas(16) float inv[2][kHeads];  // epilogue: 1 / denominator per task parity
     float sink[128];                   // the sinks of every head
+    alignas(16) uint8_t fp8_sc[kRows][16];  // e8m0 scales of the rows an fp8 tile widens, by slot
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
-    const __nv_bfloat16* kv;
+    const __nv_bfloat16* kv;   // bf16 rows (bf16 kv)
+    const uint8_t* kv8;        // e4m3 rows and their e8m0 scales (fp8 kv)
+    const uint8_t* kv_scale;
     const float* sink;
     const int32_t* idx;
     __nv_bfloat16* o;
@@ -195,6 +199,7 @@ __device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t& phase, volatile 
     return ok;
 }
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap o_map,
                    Params p) {
@@ -418,6 +423,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ncopy = __popc(m0);
                 if (copy) M.copy_list[pw][__popc(m0 & ((1u << lane) - 1u))] = make_int2(j, slot);
                 __syncwarp();
+                if constexpr (kFp8) {
+                    // e4m3 rows: chunk c's 128 codes of each listed row are staged raw in block
+                    // 2c + 1 of the row's slot (dead until the row is written), then widened in
+                    // place to bf16 in blocks 2c and 2c + 1.  Staging runs one chunk ahead of the
+                    // widening.  Lane l moves 16-code unit l % 8 of rows l / 8 + 4 i.
+                    const uint8_t* kvb8 = p.kv8 + bi * p.rows * (int64_t)kD;
+                    const uint8_t* scb = p.kv_scale + bi * p.rows * (int64_t)(kD / 32);
+                    const int unit = lane & 7;
+                    int2 ent8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int e = (lane >> 3) + 4 * i;
+                        ent8[i] = e < ncopy ? M.copy_list[pw][e] : make_int2(-1, 0);
+                    }
+#pragma unroll
+                    for (int c = 0; c <= kGroups; ++c) {
+                        if (c < kGroups) {
+                            if (ok) ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
+                            if (ok) {
+                                if (c == 0 && lane < ncopy) {  // the row's 16 scales
+                                    const int2 en = M.copy_list[pw][lane];
+                                    cp_async16(smem_addr(&M.fp8_sc[en.y][0]),
+                                               scb + (int64_t)en.x * (kD / 32), 16u);
+                                }
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    if (ent8[i].x < 0) break;
+                                    cp_async16(s_kv + (2 * c + 1) * 16384 + ent8[i].y * 128 + unit * 16,
+                                               kvb8 + (int64_t)ent8[i].x * kD + 128 * c + unit * 16, 16u);
+                                }
+                            }
+                            cp_async_commit();
+                        }
+                        if (c == 0) continue;
+                        const int cw = c - 1;  // the chunk to widen
+                        if (c < kGroups) cp_async_wait<1>(); else cp_async_wait<0>();
+                        __syncwarp();  // every lane's staged codes are visible to the warp
+                        uint4 code[8];
+                        float sc[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (ent8[i].x < 0) break;
+                            const int r = ent8[i].y;
+                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(code[i].x), "=r"(code[i].y), "=r"(code[i].z), "=r"(code[i].w)
+                                         : "r"(s_kv + (2 * cw + 1) * 16384 + r * 128 + unit * 16)
+                                         : "memory");
+                            sc[i] = fp8::e8m0_to_f32(M.fp8_sc[r][4 * cw + (unit >> 1)]);
+                        }
+                        __syncwarp();  // all codes read before any lane overwrites them
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (ent8[i].x < 0) break;
+                            const int r = ent8[i].y;
+                            uint4 lo, hi;
+                            fp8::dequant16(code[i], sc[i], lo, hi);
+                            const int u = 16 * cw + 2 * unit;  // 16-byte bf16 units u, u + 1
+                            const uint32_t row = s_kv + (u >> 3) * 16384 + r * 128;
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                             row + ((((u & 7) ^ (r & 7)) & 7) << 4)),
+                                         "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w)
+                                         : "memory");
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                             row + (((((u + 1) & 7) ^ (r & 7)) & 7) << 4)),
+                                         "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(smem_addr(&M.kv_full[cw]));
+                    }
+                    if (!ok) break;
+                    continue;
+                }
                 if (ncopy <= 2) {
                     // few new rows (e.g. the next token of a sliding window): load them into
                     // registers now, while the previous tile is still being used, and write them
@@ -796,7 +874,7 @@ bool attn_tc_supports(int h, int d, int kv_format, int64_t b, int64_t rows) {
     (void)h;
     (void)b;
     (void)rows;
-    return d == kD && kv_format == SA_KV_BF16;
+    return d == kD && (kv_format == SA_KV_BF16 || kv_format == SA_KV_FP8_E4M3);
 }
 
 size_t attn_tc_scratch_bytes(int64_t b, int64_t s, int h, int topk) {
@@ -834,7 +912,10 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
     Params p;
-    p.kv = reinterpret_cast<const __nv_bfloat16*>(c.kv);
+    const bool fp8 = c.kv_format == SA_KV_FP8_E4M3;
+    p.kv = fp8 ? nullptr : reinterpret_cast<const __nv_bfloat16*>(c.kv);
+    p.kv8 = fp8 ? reinterpret_cast<const uint8_t*>(c.kv) : nullptr;
+    p.kv_scale = fp8 ? c.kv_scale : nullptr;
     p.sink = c.sink;
     p.idx = c.idx;
     p.o = reinterpret_cast<__nv_bfloat16*>(c.o);
@@ -862,14 +943,20 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_tc_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = true;
     }
     int64_t grid = sm_count();
     if (grid > p.n_tasks) grid = p.n_tasks;
-    attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
+    if (fp8)
+        attn_tc_kernel<true><<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
+    else
+        attn_tc_kernel<false><<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || g.n_splits == 1) return e;
     return attn_combine_launch(p.part_ml, p.part_o, c.sink, c.o, n_tokens, c.h, kD, g.n_splits,

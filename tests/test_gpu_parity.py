@@ -261,12 +261,19 @@ def test_out_of_range_index_is_flagged_and_ignored(dev):
     assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what="bad idx")
 
 
-@pytest.mark.parametrize("b,s,h,topk", [(2, 9, 64, 300), (4, 1, 128, 2176), (3, 1, 64, 1152)])
-def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk, monkeypatch):
+@pytest.mark.parametrize("family", ["tcgen05", "mma"])
+@pytest.mark.parametrize("b,s,h,topk,window", [(2, 9, 64, 300, 0), (4, 1, 128, 2176, 0),
+                                               (3, 1, 64, 1152, 0), (1, 140, 64, 128, 128),
+                                               (2, 70, 64, 200, 128)])
+def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk, window, family, monkeypatch):
     """Attention over e4m3 codes + e8m0 scales gives the same bits as attention over the bf16
     round trip of the same rows (same kernel family, tiling and order)."""
-    monkeypatch.setenv("SA_FORCE_MMA", "1")
-    wl = workloads.make_random(b, s, h, 512, 2500, topk, seed=300 + topk, kv_format="fp8")
+    if family == "mma":
+        monkeypatch.setenv("SA_FORCE_MMA", "1")
+    else:
+        monkeypatch.delenv("SA_FORCE_MMA", raising=False)
+    wl = workloads.make_random(b, s, h, 512, 2500, topk, seed=300 + topk, kv_format="fp8",
+                               window=window)
     raw = _gpu.device_kv_raw(wl, dev)
     codes = torch.empty((b, wl.rows, 512), dtype=torch.uint8, device=dev)
     scales = torch.empty((b, wl.rows, 16), dtype=torch.uint8, device=dev)
