@@ -125,7 +125,7 @@ struct Params {
     int n_tiles;
     int n_splits;
     int tiles_per_split;
-    int64_t n_tasks;
+    int64_t n_units;  // (token, split) units; each is one task per head block
 };
 
 struct Task {
@@ -133,21 +133,24 @@ struct Task {
     int hb, split, t0, t1;
 };
 
-// Tasks [begin, end) of this CTA: a contiguous block, so that consecutive query tokens of one
-// sequence (which share most window rows) run back to back on the same SM.
+// A CTA serves one head block, blockIdx.x % hblocks; the CTAs of one group (blockIdx.x /
+// hblocks) serve the same (token, split) units at the same time, so every kv row a group gathers
+// is read from HBM once and from L2 by the group's other CTAs.  A group takes a contiguous block
+// of units [begin, end), so that consecutive query tokens of one sequence (which share most
+// window rows) run back to back on the same SM.
 __device__ __forceinline__ void task_range(const Params& p, int64_t& begin, int64_t& end) {
-    const int64_t g = gridDim.x, i = blockIdx.x;
-    const int64_t base = p.n_tasks / g, rem = p.n_tasks % g;
+    const int64_t g = gridDim.x / p.hblocks, i = blockIdx.x / p.hblocks;
+    const int64_t base = p.n_units / g, rem = p.n_units % g;
     begin = i * base + (i < rem ? i : rem);
     end = begin + base + (i < rem ? 1 : 0);
 }
 
+// The task of unit tau (token tau / n_splits, split tau % n_splits) for this CTA's head block.
 __device__ __forceinline__ Task task_of(const Params& p, int64_t tau) {
     Task t;
     t.split = (int)(tau % p.n_splits);
-    const int64_t th = tau / p.n_splits;
-    t.hb = (int)(th % p.hblocks);
-    t.token = th / p.hblocks;
+    t.hb = (int)(blockIdx.x % p.hblocks);
+    t.token = tau / p.n_splits;
     t.seq = t.token / p.s_len;
     t.pos = t.token - t.seq * p.s_len;
     t.t0 = t.split * p.tiles_per_split;
@@ -156,17 +159,14 @@ __device__ __forceinline__ Task task_of(const Params& p, int64_t tau) {
     return t;
 }
 
-// The task after t (splits fastest, then head blocks, then tokens), without divisions.
+// The task of the next unit (splits fastest, then tokens), without divisions.
 __device__ __forceinline__ void task_step(const Params& p, Task& t) {
     if (++t.split == p.n_splits) {
         t.split = 0;
-        if (++t.hb == p.hblocks) {
-            t.hb = 0;
-            ++t.token;
-            if (++t.pos == p.s_len) {
-                t.pos = 0;
-                ++t.seq;
-            }
+        ++t.token;
+        if (++t.pos == p.s_len) {
+            t.pos = 0;
+            ++t.seq;
         }
     }
     t.t0 = t.split * p.tiles_per_split;
@@ -422,12 +422,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, copy);
                 const int ncopy = __popc(m0);
                 if (copy) M.copy_list[pw][__popc(m0 & ((1u << lane) - 1u))] = make_int2(j, slot);
+                // the previous tile is usually still in use: pull this tile's new rows into L2
+                // now, so that the copies issued once its chunks are released hit L2
+                if (copy) {
+                    if constexpr (kFp8) {
+                        prefetch_l2(p.kv8 + (bi * p.rows + j) * (int64_t)kD, kD);
+                        prefetch_l2(p.kv_scale + (bi * p.rows + j) * (int64_t)(kD / 32), kD / 32);
+                    } else {
+                        prefetch_l2(kvb + (int64_t)j * kD, kD * 2);
+                    }
+                }
                 __syncwarp();
                 if constexpr (kFp8) {
                     // e4m3 rows: chunk c's 128 codes of each listed row are staged raw in block
                     // 2c + 1 of the row's slot (dead until the row is written), then widened in
-                    // place to bf16 in blocks 2c and 2c + 1.  Staging runs one chunk ahead of the
-                    // widening.  Lane l moves 16-code unit l % 8 of rows l / 8 + 4 i.
+                    // place to bf16 in blocks 2c and 2c + 1.  Lane l moves 16-code unit l % 8 of
+                    // rows l / 8 + 4 i.
                     const uint8_t* kvb8 = p.kv8 + bi * p.rows * (int64_t)kD;
                     const uint8_t* scb = p.kv_scale + bi * p.rows * (int64_t)(kD / 32);
                     const int unit = lane & 7;
@@ -437,28 +447,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int e = (lane >> 3) + 4 * i;
                         ent8[i] = e < ncopy ? M.copy_list[pw][e] : make_int2(-1, 0);
                     }
+                    // stage every chunk as soon as P.V has released it ...
 #pragma unroll
-                    for (int c = 0; c <= kGroups; ++c) {
-                        if (c < kGroups) {
-                            if (ok) ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
-                            if (ok) {
-                                if (c == 0 && lane < ncopy) {  // the row's 16 scales
-                                    const int2 en = M.copy_list[pw][lane];
-                                    cp_async16(smem_addr(&M.fp8_sc[en.y][0]),
-                                               scb + (int64_t)en.x * (kD / 32), 16u);
-                                }
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    if (ent8[i].x < 0) break;
-                                    cp_async16(s_kv + (2 * c + 1) * 16384 + ent8[i].y * 128 + unit * 16,
-                                               kvb8 + (int64_t)ent8[i].x * kD + 128 * c + unit * 16, 16u);
-                                }
+                    for (int c = 0; c < kGroups; ++c) {
+                        if (ok) ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
+                        if (ok) {
+                            if (c == 0 && lane < ncopy) {  // the row's 16 scales
+                                const int2 en = M.copy_list[pw][lane];
+                                cp_async16(smem_addr(&M.fp8_sc[en.y][0]),
+                                           scb + (int64_t)en.x * (kD / 32), 16u);
                             }
-                            cp_async_commit();
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                if (ent8[i].x < 0) break;
+                                cp_async16(s_kv + (2 * c + 1) * 16384 + ent8[i].y * 128 + unit * 16,
+                                           kvb8 + (int64_t)ent8[i].x * kD + 128 * c + unit * 16, 16u);
+                            }
                         }
-                        if (c == 0) continue;
-                        const int cw = c - 1;  // the chunk to widen
-                        if (c < kGroups) cp_async_wait<1>(); else cp_async_wait<0>();
+                        cp_async_commit();
+                    }
+                    // ... then widen them in order, each once its group has landed
+#pragma unroll
+                    for (int cw = 0; cw < kGroups; ++cw) {
+                        if (cw == 0) cp_async_wait<3>();
+                        else if (cw == 1) cp_async_wait<2>();
+                        else if (cw == 2) cp_async_wait<1>();
+                        else cp_async_wait<0>();
                         __syncwarp();  // every lane's staged codes are visible to the warp
                         uint4 code[8];
                         float sc[8];
@@ -929,7 +943,7 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
     p.n_tiles = g.n_tiles;
     p.n_splits = g.n_splits;
     p.tiles_per_split = g.tiles_per_split;
-    p.n_tasks = n_tokens * g.hblocks * g.n_splits;
+    p.n_units = n_tokens * g.n_splits;
     p.part_ml = nullptr;
     p.part_o = nullptr;
     if (g.n_splits > 1) {
@@ -951,8 +965,10 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = true;
     }
-    int64_t grid = sm_count();
-    if (grid > p.n_tasks) grid = p.n_tasks;
+    int64_t groups = sm_count() / g.hblocks;  // CTA groups, one CTA per head block
+    if (groups > p.n_units) groups = p.n_units;
+    if (groups < 1) groups = 1;
+    const int64_t grid = groups * g.hblocks;
     if (fp8)
         attn_tc_kernel<true><<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
     else
