@@ -45,9 +45,28 @@ DEFAULT_WORKLOAD = "swa_prefill"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 
-# dram__bytes_read.sum + dram__bytes_write.sum per sparse_attn launch, from the committed ncu
-# captures under profiles/, keyed by (library version, workload).  Absent -> null.
-NCU_TRAFFIC = {}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel (attn_tc_kernel),
+# from the ncu captures summarised under profiles/, keyed by (hash of the CUDA sources the capture
+# ran, workload).  Any change to the sources makes the key miss, so a stale figure reads as null.
+NCU_TRAFFIC = {
+    ("1802b28787086bd5", "swa_prefill"): 493_875_200,
+    ("1802b28787086bd5", "cmp_prefill"): 1_063_229_440,
+    ("1802b28787086bd5", "decode"): 82_692_096,
+}
+
+
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the sha256 over the library's CUDA sources (name + bytes, sorted)."""
+    import glob
+    import hashlib
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "sparse_latent_attention_gb300",
+                        "csrc")
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 # --------------------------------------------------------------------------------------------
@@ -359,7 +378,8 @@ def run_gpu(args, rank, world, local):
     gbs = terms["alg_bytes"] / t_attn / 1e9
     tfs = terms["flops"] / t_attn / 1e12
     lib_version = path.sa._lib.version()
-    traffic = NCU_TRAFFIC.get((lib_version, wl.name))
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get((src_hash, wl.name))
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic}
@@ -395,6 +415,7 @@ def run_gpu(args, rank, world, local):
         "gpu_launches": path.launches_per_step * args.steps,
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "lib_version": lib_version,
+        "kernel_source_hash": src_hash,
     }
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
