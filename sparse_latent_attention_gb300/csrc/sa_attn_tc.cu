@@ -72,10 +72,10 @@ constexpr uint32_t kPBytes = kRows * kHeads * 2;  // 16 KB: [128 rows x 128 B]
 constexpr uint32_t kOffKv = 0;
 constexpr uint32_t kOffQ = kOffKv + kKvBytes;
 constexpr uint32_t kOffP = kOffQ + kQBytes;
-// o staging: [32 heads x 64 d] boxes of 128-byte rows, 128-byte swizzle, one per 64 d of a chunk
-constexpr uint32_t kStageBoxBytes = 32 * 128;
+// o staging: one [32 heads x 32 d] box of 64-byte rows (no swizzle) per epilogue warp
+constexpr uint32_t kStageBoxBytes = 32 * 64;
 constexpr uint32_t kOffStage = kOffP + kPBytes;
-constexpr uint32_t kOffMisc = kOffStage + 2 * kStageBoxBytes;
+constexpr uint32_t kOffMisc = kOffStage + 4 * kStageBoxBytes;
 
 struct Misc {
     uint64_t q_full, q_empty;
@@ -191,6 +191,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// mbar_wait by every lane of a converged warp, with a warp-uniform result.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
 // Barrier among the 128 threads of one warpgroup, on an mbarrier so that it is bounded.
 __device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t& phase, volatile int* abort) {
     mbar_arrive(bar);
@@ -271,7 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------------ MMA issue
-        if (lane == 0) {
+        // The whole warp runs this loop (descriptors stay in uniform registers); each MMA and
+        // commit is issued by one elected lane, and every lane waits on the barriers.  A wait's
+        // result is made warp-uniform so that a time-out cannot split the warp.
+        {
             constexpr uint32_t id_s = idesc_bf16_f32(kRows, kHeads, false, false);
             constexpr uint32_t id_o = idesc_bf16_f32(kRows, kHeads, true, true);
             constexpr uint32_t id_l = idesc_bf16_f32(kRows, kHeads, false, true);
@@ -287,68 +295,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
                 const uint32_t kp = (uint32_t)(k & 1);
                 if (t.t0 == t.t1) {  // nothing listed for this task: keep every phase in step
-                    ok = mbar_wait(smem_addr(&M.q_full), kp, abort);
-                    mma_commit(smem_addr(&M.q_empty));
+                    ok = warp_wait(smem_addr(&M.q_full), kp, abort);
+                    mma_commit_elect(smem_addr(&M.q_empty));
                     for (int c = 0; c < kGroups && ok; ++c)
-                        ok = mbar_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort);
-                    mma_commit(smem_addr(&M.o_full));
+                        ok = warp_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort);
+                    mma_commit_elect(smem_addr(&M.o_full));
                     continue;
                 }
                 for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
                     const uint32_t b = T & 1, use = (T >> 1) & 1, tp = T & 1;
                     const uint32_t s_col = tmem + kColS + 64 * b;
                     // S^T = KV . Q^T: every wait first, then the 32 MMAs back to back
-                    ok = mbar_wait(smem_addr(&M.s_empty[b]), use ^ 1, abort);
-                    if (ok && ti == t.t0) ok = mbar_wait(smem_addr(&M.q_full), kp, abort);
+                    ok = warp_wait(smem_addr(&M.s_empty[b]), use ^ 1, abort);
+                    if (ok && ti == t.t0) ok = warp_wait(smem_addr(&M.q_full), kp, abort);
                     if (!ok) break;
                     // K step ks (16 of 512): block ks / 4 of the tile / Q, 32 B per step inside
                     // a 128-byte row (2 in the descriptor's 16-byte address units); each 128-d
                     // chunk of the tile as soon as it has landed
 #pragma unroll
                     for (int c = 0; c < kGroups; ++c) {
-                        if (!(ok = mbar_wait(smem_addr(&M.kv_full[c]), tp, abort))) break;
+                        if (!(ok = warp_wait(smem_addr(&M.kv_full[c]), tp, abort))) break;
                         tc_fence_after();
 #pragma unroll
                         for (int ks = 8 * c; ks < 8 * c + 8; ++ks)
-                            mma_bf16_ss(s_col, a_s0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                            mma_bf16_ss_elect(s_col, a_s0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
                                         b_s0 + (uint64_t)((ks >> 2) * 512 + (ks & 3) * 2), id_s,
                                         ks != 0);
                     }
                     if (!ok) break;
-                    if (ti == t.t1 - 1) mma_commit(smem_addr(&M.q_empty));
-                    mma_commit(smem_addr(&M.s_full[b]));
+                    if (ti == t.t1 - 1) mma_commit_elect(smem_addr(&M.q_empty));
+                    mma_commit_elect(smem_addr(&M.s_full[b]));
                     // O^T += KV^T . P^T
-                    ok = mbar_wait(smem_addr(&M.p_full), tp, abort);
+                    ok = warp_wait(smem_addr(&M.p_full), tp, abort);
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < kGroups; ++c) {
                         if (ti == t.t0) {  // the epilogue has read this chunk of the last task's O
-                            if (!(ok = mbar_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort))) break;
+                            if (!(ok = warp_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort))) break;
                             tc_fence_after();
                         }
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)  // 16 rows = 2 KB per K step
-                            mma_bf16_ss(tmem + kColO + 64 * c, a_o0 + (uint64_t)(c * 2048 + ks * 128),
+                            mma_bf16_ss_elect(tmem + kColO + 64 * c, a_o0 + (uint64_t)(c * 2048 + ks * 128),
                                         b_o0 + (uint64_t)(ks * 128), id_o, !(ti == t.t0 && ks == 0));
-                        mma_commit(smem_addr(&M.kv_empty[c]));  // chunk c of the tile is read
+                        mma_commit_elect(smem_addr(&M.kv_empty[c]));  // chunk c of the tile is read
                     }
                     if (!ok) break;
                     // l += ones . P^T (every element of the A operand is 1, so one 8-column
                     // block of TMEM serves every K step)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ts(tmem + kColSum, tmem + kColOnes, b_o0 + (uint64_t)(ks * 128),
+                        mma_bf16_ts_elect(tmem + kColSum, tmem + kColOnes, b_o0 + (uint64_t)(ks * 128),
                                     id_l, !(ti == t.t0 && ks == 0));
-                    mma_commit(smem_addr(&M.p_empty));
-                    if (ti == t.t1 - 1) mma_commit(smem_addr(&M.o_full));
+                    mma_commit_elect(smem_addr(&M.p_empty));
+                    if (ti == t.t1 - 1) mma_commit_elect(smem_addr(&M.o_full));
                 }
             }
             // let every issued MMA finish before the accumulators are released
-            mma_commit(smem_addr(&M.done));
-            mbar_wait(smem_addr(&M.done), 0, abort);
+            mma_commit_elect(smem_addr(&M.done));
+            warp_wait(smem_addr(&M.done), 0, abort);
         }
-        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------------ Q loads (TMA)
         if (lane == 0) {
@@ -714,19 +721,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------------ epilogue
         // O^T chunk c (128 d x 64 heads) leaves TMEM at once (the MMA may refill it), is scaled by
-        // 1 / denominator, packed to bf16 and transposed through a swizzled shared-memory stage
-        // that TMA stores to o (one [32 heads x 64 d] box per 64 d).  Every thread passes every
-        // barrier of a task, even after a failed wait, so the warpgroup's barriers never split.
+        // 1 / denominator and packed to bf16.  Each warp (32 d) transposes its part through its
+        // own [32 heads x 32 d] shared-memory box and stores it to o with TMA, synchronising only
+        // with itself.  Every thread passes every barrier of a task, even after a failed wait, so
+        // the warpgroup's barriers never split.
         const int q4 = warp & 3;
         const int et = tid - 32 * kWarpEpilogue;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        // stage address of this thread's d pair: box q4 / 2, 16-byte unit st_unit of the
-        // 128-byte row (before the swizzle), byte 4 (k & 3) inside it
-        const uint32_t s_stage = smem_addr(smem + kOffStage);
+        // this warp's box: 32 rows (heads) of 64 bytes (32 d); this thread's word in a row holds
+        // the d pair 2 (lane / 2), 2 (lane / 2) + 1
+        const uint32_t s_box = smem_addr(smem + kOffStage) + q4 * kStageBoxBytes;
         const int odd = lane & 1;
         const uint32_t sel = odd ? 0x3276u : 0x5410u;
-        const uint32_t st_unit = 4 * (q4 & 1) + (lane >> 3);
-        const uint32_t st_base = s_stage + (q4 >> 1) * kStageBoxBytes + 4 * ((lane >> 1) & 3);
+        const uint32_t st_base = s_box + 4 * (lane >> 1) + 64 * odd;
         int64_t k = 0;
         bool ok = true;
         Task t = task_of(p, tb);
@@ -782,43 +789,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int rh = 0; rh < 2; ++rh) {  // heads 32 rh .. 32 rh + 31 of the block
-                    // Lanes 2k and 2k+1 hold d = 2k and 2k+1 of every head.  Two heads a and
-                    // a + 4 are packed per word, the neighbours swap words, and the even lane
-                    // keeps head a's (d, d+1) pair, the odd lane head a + 4's.  Rows a and a + 4
-                    // of the swizzled box sit in opposite 64-byte halves of the banks.
+                    // Lanes 2k and 2k + 1 hold d = 2k and 2k + 1 of every head.  Heads a and a + 1
+                    // are packed per word, the neighbours swap words, and the even lane keeps head
+                    // a's (d, d + 1) pair, the odd lane head a + 1's: rows a and a + 1 of the box
+                    // are 64 bytes apart, in opposite halves of the banks.  (O^T is always finite,
+                    // so a head with inv = 0 comes out as zeros.)
+                    uint32_t out[16];
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const float4 wa = *reinterpret_cast<const float4*>(&M.inv[kpar][32 * rh + 8 * m]);
-                        const float4 wb = *reinterpret_cast<const float4*>(&M.inv[kpar][32 * rh + 8 * m + 4]);
-                        const float fa[4] = {wa.x, wa.y, wa.z, wa.w}, fb[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int a = 32 * rh + 8 * m + i;
-                            const float va = fa[i] > 0.f ? __uint_as_float(r[a]) * fa[i] : 0.f;
-                            const float vb = fb[i] > 0.f ? __uint_as_float(r[a + 4]) * fb[i] : 0.f;
-                            const uint32_t pk = pack_bf16(va, vb);
-                            const uint32_t x = __shfl_xor_sync(0xffffffffu, pk, 1);
-                            const uint32_t row = 8 * m + i + 4 * odd;
-                            st_shared_b32(st_base + row * 128 + (((st_unit ^ row) & 7) << 4),
-                                          __byte_perm(pk, x, sel));
-                        }
+                    for (int m = 0; m < 8; ++m) {
+                        const float4 w = *reinterpret_cast<const float4*>(&M.inv[kpar][32 * rh + 4 * m]);
+                        const int a = 32 * rh + 4 * m;
+                        const uint32_t pk0 = pack_bf16(__uint_as_float(r[a]) * w.x,
+                                                       __uint_as_float(r[a + 1]) * w.y);
+                        const uint32_t pk1 = pack_bf16(__uint_as_float(r[a + 2]) * w.z,
+                                                       __uint_as_float(r[a + 3]) * w.w);
+                        out[2 * m] = __byte_perm(pk0, __shfl_xor_sync(0xffffffffu, pk0, 1), sel);
+                        out[2 * m + 1] = __byte_perm(pk1, __shfl_xor_sync(0xffffffffu, pk1, 1), sel);
                     }
+                    // the box is free once this warp's previous store has read it
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) st_shared_b32(st_base + 128 * j, out[j]);
                     fence_proxy_async_smem();
-                    named_barrier(1, 128);
-                    if (et == 0) {
-                        if (ok && h0 + 32 * rh < p.h) {
-                            const int32_t y = h0 + 32 * rh, z = (int32_t)t.token;
-                            tma_store_3d(&o_map, s_stage, 128 * c, y, z);
-                            tma_store_3d(&o_map, s_stage + kStageBoxBytes, 128 * c + 64, y, z);
-                            bulk_commit();
-                        }
-                        bulk_wait_read_all();  // the stage may be rewritten
+                    __syncwarp();
+                    if (lane == 0 && ok && h0 + 32 * rh < p.h) {
+                        tma_store_3d(&o_map, s_box, 128 * c + 32 * q4, h0 + 32 * rh,
+                                     (int32_t)t.token);
+                        bulk_commit();
                     }
-                    named_barrier(1, 128);
                 }
             }
         }
-        if (et == 0) bulk_wait_all();
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -914,14 +917,14 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    // o as [tokens][h][512]: a [1 x 32 x 64] box is clipped at h for a partial head block
+    // o as [tokens][h][512]: a [1 x 32 x 32] box is clipped at h for a partial head block
     CUtensorMap omap;
     const cuuint64_t odim[3] = {(cuuint64_t)kD, (cuuint64_t)c.h, (cuuint64_t)n_tokens};
     const cuuint64_t ostride[2] = {(cuuint64_t)kD * 2, (cuuint64_t)c.h * kD * 2};
-    const cuuint32_t obox[3] = {64, (cuuint32_t)(c.h < 32 ? c.h : 32), 1};
+    const cuuint32_t obox[3] = {32, (cuuint32_t)(c.h < 32 ? c.h : 32), 1};
     const cuuint32_t oestride[3] = {1, 1, 1};
     r = encode(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c.o, odim, ostride, obox, oestride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
