@@ -96,7 +96,7 @@ struct Misc {
     float colred[4][kHeads];           // per-warp column max of the current tile
     float suml[kHeads];                // epilogue: the task's denominators read from TMEM
     float m[kHeads];                   // running max (log2 units)
-    float mu[kHeads];                  // the running max with -inf replaced by 0
+    alignas(16) float mu[kHeads];      // the running max with -inf replaced by 0
     float alpha[kHeads];               // rescale factor of this tile
     float stats_m[2][kHeads];          // final max (0 when none) per task parity
     alignas(16) float inv[2][kHeads];  // epilogue: 1 / denominator per task parity
@@ -616,22 +616,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(smem_addr(&M.kv_full[0]), tp, abort);  // the tile's row ids
                 if (ok) ok = mbar_wait(smem_addr(&M.s_full[b]), use, abort);
                 if (!ok) break;
+                // an empty slot's logits become -inf (pass 1) and its P^T row zeros (pass 2)
                 const bool valid = M.row_id[tp][row] >= 0;
+                const float row_bias = valid ? 0.f : -INFINITY;
+                const uint32_t row_mask = valid ? 0xFFFFFFFFu : 0u;
                 const uint32_t s_addr = tmem + lane_base + kColS + 64 * b;
                 tc_fence_after();
-                // pass 1: column maximum of the scaled logits over the 128 rows (two halves)
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(s_addr + 32 * half, r);
+                // pass 1: column maximum of the scaled logits over the 128 rows; lane i keeps the
+                // warp maxima of heads i and 32 + i
+                {
+                    uint32_t r[kHeads];
+                    tmem_ld_32x32b_x64(s_addr, r);
                     tmem_wait_ld();
+                    float mine0 = -INFINITY, mine1 = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {  // warp max per head, one lane stores it
-                        const float x = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                    for (int i = 0; i < kHeads; ++i) {
+                        const float x = fmaf(__uint_as_float(r[i]), p.scale_log2, row_bias);
                         float mx;
                         asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(x));
-                        if (lane == i) M.colred[q4][32 * half + i] = mx;
+                        if (i < 32) {
+                            if (lane == i) mine0 = mx;
+                        } else {
+                            if (lane == i - 32) mine1 = mx;
+                        }
                     }
+                    M.colred[q4][lane] = mine0;
+                    M.colred[q4][32 + lane] = mine1;
                 }
                 if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
                 if (row < kHeads) {
@@ -677,29 +687,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                 }
-                // pass 2 (two halves): p = 2^(x - m) as the P^T row (128-byte swizzled MN-major
-                // operand), and this tile's column sums, folded in at the next tile / task end
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float pr[32];
-                    {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(s_addr + 32 * half, r);
-                        tmem_wait_ld();
-                        const float* mu = &M.mu[32 * half];
+                // pass 2: p = 2^(x - m) as the P^T row (128-byte swizzled MN-major operand); the
+                // sums are accumulated by the tensor core from P^T
+                {
+                    uint32_t r[kHeads];
+                    tmem_ld_32x32b_x64(s_addr, r);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            pr[i] = valid ? fast_exp2(__uint_as_float(r[i]) * p.scale_log2 - mu[i]) : 0.f;
-                    }
+                    for (int u = 0; u < 8; ++u) {  // 16-byte unit u of the row: heads 8u .. 8u + 7
+                        const float4 ma = *reinterpret_cast<const float4*>(&M.mu[8 * u]);
+                        const float4 mb = *reinterpret_cast<const float4*>(&M.mu[8 * u + 4]);
+                        const float mu8[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                        float e[8];
 #pragma unroll
-                    for (int u4 = 0; u4 < 4; ++u4) {
-                        const uint32_t u = 4 * half + u4;
+                        for (int i = 0; i < 8; ++i)
+                            e[i] = fast_exp2(fmaf(__uint_as_float(r[8 * u + i]), p.scale_log2, -mu8[i]));
                         const uint32_t dst = s_p + row * 128 + (((u ^ (row & 7)) & 7) << 4);
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                                     "r"(pack_bf16(pr[8 * u4], pr[8 * u4 + 1])),
-                                     "r"(pack_bf16(pr[8 * u4 + 2], pr[8 * u4 + 3])),
-                                     "r"(pack_bf16(pr[8 * u4 + 4], pr[8 * u4 + 5])),
-                                     "r"(pack_bf16(pr[8 * u4 + 6], pr[8 * u4 + 7])));
+                                     "r"(pack_bf16(e[0], e[1]) & row_mask),
+                                     "r"(pack_bf16(e[2], e[3]) & row_mask),
+                                     "r"(pack_bf16(e[4], e[5]) & row_mask),
+                                     "r"(pack_bf16(e[6], e[7]) & row_mask));
                     }
                 }
                 tc_fence_before();
