@@ -311,8 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     // K step ks (16 of 512): block ks / 4 of the tile / Q, 32 B per step inside
                     // a 128-byte row (2 in the descriptor's 16-byte address units); each 128-d
-                    // chunk of the tile as soon as it has landed
-#pragma unroll
+                    // chunk of the tile as soon as it has landed (the chunk loop is kept rolled: the
+                    // issuing warp shares its instruction cache with three other roles)
+#pragma unroll 1
                     for (int c = 0; c < kGroups; ++c) {
                         if (!(ok = warp_wait(smem_addr(&M.kv_full[c]), tp, abort))) break;
                         tc_fence_after();
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = warp_wait(smem_addr(&M.p_full), tp, abort);
                     if (!ok) break;
                     tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < kGroups; ++c) {
                         if (ti == t.t0) {  // the epilogue has read this chunk of the last task's O
                             if (!(ok = warp_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort))) break;
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ncopy <= 2) {
                     // few new rows (e.g. the next token of a sliding window): load them into
                     // registers now, while the previous tile is still being used, and write them
-                    // to their slots once the whole tile is released
+                    // to their slots chunk by chunk as the tile is released
                     uint4 v[2][2];
                     int2 ent[2];
 #pragma unroll
@@ -532,28 +533,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v[e][1] = __ldg(src + 32 + lane);
                         }
                     }
-#pragma unroll 1
-                    for (int c = 0; c < kGroups && ok; ++c)
-                        ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
-                    if (!ok) break;
+                    // chunk c (units 16 c .. 16 c + 15) is held by the lanes with lane / 16 ==
+                    // c % 2, in v[.][c / 2]; each chunk is written and signalled as soon as P.V
+                    // has released it
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        if (ent[e].x < 0) continue;
-                        const int r = ent[e].y;
+                    for (int c = 0; c < kGroups; ++c) {
+                        if (ok) ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
+                        if (ok && (lane >> 4) == (c & 1)) {
 #pragma unroll
-                        for (int hv = 0; hv < 2; ++hv) {
-                            const int u = 32 * hv + lane;  // 16-byte unit of the 1 KB row
-                            const uint32_t dst = s_kv + (u >> 3) * 16384 + r * 128 +
-                                                 ((((u & 7) ^ (r & 7)) & 7) << 4);
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                                         "r"(v[e][hv].x), "r"(v[e][hv].y), "r"(v[e][hv].z),
-                                         "r"(v[e][hv].w)
-                                         : "memory");
+                            for (int e = 0; e < 2; ++e) {
+                                if (ent[e].x < 0) continue;
+                                const int r = ent[e].y;
+                                const int u = 32 * (c >> 1) + lane;  // 16-byte unit of the 1 KB row
+                                const uint4 w = v[e][c >> 1];
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                                 s_kv + (u >> 3) * 16384 + r * 128 +
+                                                 ((((u & 7) ^ (r & 7)) & 7) << 4)),
+                                             "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
+                                             : "memory");
+                            }
                         }
+                        fence_proxy_async_smem();
+                        mbar_arrive(smem_addr(&M.kv_full[c]));
                     }
-                    fence_proxy_async_smem();
-#pragma unroll
-                    for (int c = 0; c < kGroups; ++c) mbar_arrive(smem_addr(&M.kv_full[c]));
+                    if (!ok) break;
                     continue;
                 }
                 // this lane's rows of the list: entries lane / 16 + 2 i (two rows per instruction)
