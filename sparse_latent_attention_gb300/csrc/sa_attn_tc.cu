@@ -94,12 +94,11 @@ struct Misc {
     int64_t tile_seq[2];               // sequence whose rows a tile holds (-1 = none)
     int2 copy_list[kProdWarps][32];    // per producer warp: (kv row, slot) of the rows to copy
     float colred[4][kHeads];           // per-warp column max of the current tile
-    float suml[kHeads];                // epilogue: the task's denominators read from TMEM
     float m[kHeads];                   // running max (log2 units)
     alignas(16) float mu[kHeads];      // the running max with -inf replaced by 0
     float alpha[kHeads];               // rescale factor of this tile
     float stats_m[2][kHeads];          // final max (0 when none) per task parity
-    alignas(16) float inv[2][kHeads];  // epilogue: 1 / denominator per task parity
+    alignas(16) float inv[4][kHeads];  // epilogue: 1 / denominator, a table per epilogue warp
     float sink[128];                   // the sinks of every head
     alignas(16) uint8_t fp8_sc[kRows][16];  // e8m0 scales of the rows an fp8 tile widens, by slot
 };
@@ -757,31 +756,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool split = p.n_splits > 1;
             const int64_t pbase = (t.token * p.n_splits + t.split) * (int64_t)p.h + h0;
-            // the denominators: every TMEM lane of the sum block holds the same row sums
-            if (q4 < 2) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kColSum + 32 * q4, r);
-                tmem_wait_ld();
+            // the denominators: every TMEM lane of the sum block holds the same row sums, so
+            // each warp reads them all and lane l finishes heads l and l + 32 into the warp's own
+            // table (no barrier across the warps)
+            {
+                float lsum[2];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (lane == i) M.suml[32 * q4 + i] = t.t1 > t.t0 ? __uint_as_float(r[i]) : 0.f;
-            }
-            named_barrier(1, 128);
-            if (et < kHeads) {
-                const int h = et;
-                const float l = M.suml[h], mu = M.stats_m[kpar][h];
-                float inv = 0.f;
-                if (ok && h < hc) {
-                    if (split) {
-                        p.part_ml[(pbase + h) * 2 + 0] = mu;
-                        p.part_ml[(pbase + h) * 2 + 1] = l;
-                    } else if (l > 0.f) {
-                        inv = 1.f / (l + fast_exp2(M.sink[h0 + h] * kLog2e - mu));
-                    }
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem + lane_base + kColSum + 32 * hh, r);
+                    tmem_wait_ld();
+                    float v = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (lane == i) v = __uint_as_float(r[i]);
+                    lsum[hh] = t.t1 > t.t0 ? v : 0.f;
                 }
-                M.inv[kpar][h] = inv;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int h = lane + 32 * hh;
+                    const float l = lsum[hh], mu = M.stats_m[kpar][h];
+                    float inv = 0.f;
+                    if (ok && h < hc) {
+                        if (split) {
+                            if (q4 == 0) {
+                                p.part_ml[(pbase + h) * 2 + 0] = mu;
+                                p.part_ml[(pbase + h) * 2 + 1] = l;
+                            }
+                        } else if (l > 0.f) {
+                            inv = 1.f / (l + fast_exp2(M.sink[h0 + h] * kLog2e - mu));
+                        }
+                    }
+                    M.inv[q4][h] = inv;
+                }
+                __syncwarp();
             }
-            named_barrier(1, 128);
 #pragma unroll 1
             for (int c = 0; c < kGroups; ++c) {
                 uint32_t r[kHeads];
@@ -808,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t out[16];
 #pragma unroll
                     for (int m = 0; m < 8; ++m) {
-                        const float4 w = *reinterpret_cast<const float4*>(&M.inv[kpar][32 * rh + 4 * m]);
+                        const float4 w = *reinterpret_cast<const float4*>(&M.inv[q4][32 * rh + 4 * m]);
                         const int a = 32 * rh + 4 * m;
                         const uint32_t pk0 = pack_bf16(__uint_as_float(r[a]) * w.x,
                                                        __uint_as_float(r[a + 1]) * w.y);
