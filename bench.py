@@ -49,9 +49,9 @@ L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 # from the ncu captures summarised under profiles/, keyed by (hash of the CUDA sources the capture
 # ran, workload).  Any change to the sources makes the key miss, so a stale figure reads as null.
 NCU_TRAFFIC = {
-    ("1802b28787086bd5", "swa_prefill"): 493_875_200,
-    ("1802b28787086bd5", "cmp_prefill"): 1_063_229_440,
-    ("1802b28787086bd5", "decode"): 82_692_096,
+    ("88a28cbac99e2795", "swa_prefill"): 501_384_704,
+    ("88a28cbac99e2795", "cmp_prefill"): 1_068_094_976,
+    ("88a28cbac99e2795", "decode"): 83_754_496,
 }
 
 
