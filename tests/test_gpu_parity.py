@@ -198,6 +198,10 @@ RANDOM_CASES = [
     (2, 7, 64, 512, 400, 130, dict(q_scale=12.0)),  # large logits: running max moves a lot
     (1, 8, 64, 512, 100, 100, dict(sink_scale=30.0)),  # sinks far from the logits
     (2, 9, 16, 128, 50, 40, dict(neg_frac=0.97)),   # nearly everything masked
+    # head_dim 512 (tcgen05 path) with partial head blocks: o's TMA store boxes clipped at h
+    (2, 9, 100, 512, 300, 200, {}),                 # 64 + 36 heads, two tiles
+    (1, 12, 8, 512, 200, 130, {}),                  # fewer heads than one 32-row store box
+    (3, 1, 40, 512, 2000, 600, {}),                 # decode split with a partial head block
 ]
 
 
@@ -264,7 +268,7 @@ def test_out_of_range_index_is_flagged_and_ignored(dev):
 @pytest.mark.parametrize("family", ["tcgen05", "mma"])
 @pytest.mark.parametrize("b,s,h,topk,window", [(2, 9, 64, 300, 0), (4, 1, 128, 2176, 0),
                                                (3, 1, 64, 1152, 0), (1, 140, 64, 128, 128),
-                                               (2, 70, 64, 200, 128)])
+                                               (2, 70, 64, 200, 128), (2, 5, 40, 300, 0)])
 def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk, window, family, monkeypatch):
     """Attention over e4m3 codes + e8m0 scales gives the same bits as attention over the bf16
     round trip of the same rows (same kernel family, tiling and order)."""
