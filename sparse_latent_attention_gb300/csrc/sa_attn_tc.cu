@@ -4,35 +4,40 @@
 // and the precision paragraph; "DeepSeek V4.1" attention page, Attention.forward.
 //
 // Formulation.  All heads of a query token read the same gathered kv rows, and the rows serve as
-// both keys and values.  With head_dim 512 an f32 accumulator of O for 64 heads needs 256 TMEM
-// columns in any orientation, while with heads as the MMA's M dimension O takes all 512 columns
-// (the full TMEM) and leaves no room for the logits.  So the gathered rows are the M dimension:
-//   S^T[128 rows x 64 heads]  = KV_tile[128 x 512] . Q^T            (4 x 8 MMAs, K = 512)
-//   O^T[512 x 64 heads]      += KV_tile^T[512 x 128] . P^T[128 x 64] (4 M-chunks x 8 MMAs)
-// TMEM holds O^T (256 columns), two S^T buffers (2 x 64), an all-ones bf16 operand (8 columns)
-// and the softmax denominators (64 columns): l = ones . P^T is one more MMA per K step, so the
-// row sums come from the same bf16 P that multiplies V and are rescaled together with O.  The same swizzled shared-memory
-// tile is the K-major A operand of the first product and the MN-major A operand of the second.
-// The softmax runs down the columns of S^T (one TMEM lane = one gathered row per thread): the
-// column maximum is a warp max reduction plus a 4-warp exchange, and a running maximum is only
-// raised (and O rescaled) when a new logit exceeds it by more than 2^8, so the rescale is rare.
-// The sink joins the denominator once, in the epilogue: o = O / (l + 2^(sink log2e - m)).
+// both keys and values.  Rows are gathered 64 at a time (a tile) into one of two shared-memory
+// buffers, so that one tile is gathered while the tensor core works on the other:
+//   S[64 heads x 64 rows]   = Q[64 x 512] . KV_tile^T                   (32 MMAs, M = 64)
+//   O^T[512 x 64 heads]    += KV_tile^T[512 x 64] . P^T[64 rows x 64]    (4 M-chunks x 4 MMAs)
+// With head_dim 512 an f32 accumulator of O for 64 heads needs 256 TMEM columns; as O^T (d on
+// the lanes) it leaves the other 256 columns for two S buffers.  S has the heads as its M
+// dimension, and an M = 64 accumulator puts head 16 w + i on TMEM lane 32 w + i: a softmax
+// thread owns one head and half of the tile's columns (the other half sits with the thread 16
+// lanes up), so the row maximum and sum need one shuffle and no exchange across warps.  The
+// same swizzled shared-memory tile is the K-major B operand of the first product and the
+// MN-major A operand of the second; P (bf16) is the K-major B operand of the second.  A
+// running maximum is only raised (and O rescaled) when a new logit exceeds it by more than 2^8,
+// so the rescale is rare.  The sink joins the denominator once, in the epilogue:
+// o = O / (l + 2^(sink log2e - m)).
 //
-// Roles (persistent CTAs, one 64-head block of one query token per task, 384 threads):
-//   warp 0      MMA issue (one thread) and TMEM allocation
-//   warp 1      Q loads (TMA, 128-byte swizzle)
-//   warps 2-3   kv row gather (cp.async 16 B, swizzled in place; rows already resident from the
-//               previous tile are kept -- see below)
-//   warps 4-7   softmax: S^T -> P^T (bf16, shared memory), running max, O rescale
-//   warps 8-11  epilogue: O^T -> o (bf16) or split partials
+// Roles (persistent CTAs, one 64-head block of one query token per task, 448 threads):
+//   warp 0      MMA issue (one elected lane) and TMEM allocation; the P.V of a tile is issued
+//               before the logits of the next, so that the gather of a buffer overlaps the
+//               softmax and P.V of the other
+//   warp 1      Q loads (TMA, 128-byte swizzle) and an L2 prefetch of the next task's Q
+//   warps 2-5   kv row gather: the 128 idx columns of a pair of tiles at a time, one per thread;
+//               cp.async 16 B into the swizzled layout (fp8 rows are staged raw and widened in
+//               place); rows already resident from the previous pair are kept -- see below
+//   warps 6-9   softmax: S -> P (bf16, shared memory), running max and sum, O rescale
+//   warps 10-13 epilogue: O^T -> o (bf16) or split partials
 // Every wait is bounded; a wait that gives up raises the timeout bit and every role unwinds.
 //
 // Row placement.  The order of the gathered rows inside a tile does not matter (the softmax and
-// P.V sum over rows; masking uses the recorded row id of each slot).  When the valid rows of a
-// tile have distinct residues mod 128, row j goes to slot j mod 128; otherwise row r of the tile
-// goes to slot r.  A row already sitting in its slot from the previous tile is not copied again.
-// A CTA takes a contiguous block of tasks, so consecutive query tokens of a sliding window (127
-// of 128 rows shared) reload one row per token.
+// P.V sum over rows; masking uses each tile's set of claimed slots).  The 128 idx columns of a
+// pair of tiles are placed together: when their valid rows have distinct residues mod 128, row
+// j goes to slot j mod 128 (slots 0-63 in the pair's first tile, 64-127 in its second);
+// otherwise column r of the pair goes to slot r.  A row already sitting in its slot from the
+// previous pair is not copied again.  A CTA takes a contiguous block of tasks, so consecutive
+// query tokens of a sliding window (127 of 128 rows shared) reload one row per token.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -52,60 +57,61 @@ namespace {
 using namespace tc;
 
 constexpr int kD = 512;           // head_dim handled by this kernel
-constexpr int kRows = 128;        // gathered rows per tile (MMA M)
-constexpr int kHeads = 64;        // heads per task (MMA N)
-constexpr int kGroups = 4;        // 128-wide d groups (pipeline granularity)
-constexpr int kProdWarps = 4;                      // kv gather warps (one tile slot per thread)
-constexpr int kProdThreads = 32 * kProdWarps;
+constexpr int kRows = 64;         // gathered rows per tile (N of the logits, K of P.V)
+constexpr int kHeads = 64;        // heads per task (M of the logits, N of P.V)
+constexpr int kChunks = 4;        // 128-d chunks of O^T (M of P.V)
+constexpr int kProdWarps = 4;                       // kv gather warps (one pair column per thread)
+constexpr int kProdThreads = 32 * kProdWarps;       // = the 128 columns of a pair of tiles
 constexpr int kWarpSoftmax = 2 + kProdWarps;        // first softmax warp
 constexpr int kWarpEpilogue = kWarpSoftmax + 4;     // first epilogue warp
 constexpr int kThreads = 32 * (kWarpEpilogue + 4);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// TMEM columns: O^T chunks, the two S^T buffers, the all-ones operand, the row sums
-constexpr uint32_t kColO = 0, kColS = 256, kColOnes = 384, kColSum = 448;
+// TMEM columns: O^T chunks (4 x 64), the two S buffers (2 x 64)
+constexpr uint32_t kColO = 0, kColS = 256;
 
 // Shared-memory map (dynamic, 1024-byte aligned base)
-constexpr uint32_t kKvBytes = kRows * kD * 2;     // 128 KB: 8 blocks of [128 rows x 128 B]
+constexpr uint32_t kBlkBytes = kRows * 128;       // 8 KB: [64 rows x 64 d] with 128-byte rows
+constexpr uint32_t kBufBytes = 8 * kBlkBytes;     // 64 KB: one tile, 8 blocks of 64 d
 constexpr uint32_t kQBytes = kHeads * kD * 2;     // 64 KB: 8 blocks of [64 heads x 128 B]
-constexpr uint32_t kPBytes = kRows * kHeads * 2;  // 16 KB: [128 rows x 128 B]
+constexpr uint32_t kPBytes = kHeads * kRows * 2;  // 8 KB: [64 heads x 128 B] per P buffer
 constexpr uint32_t kOffKv = 0;
-constexpr uint32_t kOffQ = kOffKv + kKvBytes;
+constexpr uint32_t kOffQ = kOffKv + 2 * kBufBytes;
 constexpr uint32_t kOffP = kOffQ + kQBytes;
 // o staging: one [32 heads x 32 d] box of 64-byte rows (no swizzle) per epilogue warp
 constexpr uint32_t kStageBoxBytes = 32 * 64;
-constexpr uint32_t kOffStage = kOffP + kPBytes;
+constexpr uint32_t kOffStage = kOffP + 2 * kPBytes;
 constexpr uint32_t kOffMisc = kOffStage + 4 * kStageBoxBytes;
 
 struct Misc {
     uint64_t q_full, q_empty;
-    uint64_t kv_full[kGroups], kv_empty[kGroups];  // per 128-d chunk of the kv tile
-    uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, p_empty;
-    uint64_t o_full, o_empty[kGroups];
-    uint64_t stats_full[2];
-    uint64_t sm_bar, ep_bar, pr_bar, done;
+    uint64_t kv_full[2], kv_empty[2];  // per kv buffer
+    uint64_t s_full[2], s_empty[2];    // per S buffer (TMEM)
+    uint64_t p_full[2], p_empty[2];    // per P buffer (shared memory)
+    uint64_t o_full, o_empty[kChunks];
+    uint64_t stats_full[2], stats_empty[2];
+    uint64_t sm_bar, pr_bar, done;
     uint32_t tmem_base;
     int abort;
-    int need_corr[2];
-    int row_id[2][kRows];              // kv row held by each slot per tile parity, -1 = none
-    uint32_t ring_bits[2][4];          // residues mod 128 of a tile's valid rows
-    int ring_count[2];                 // number of valid rows of a tile
-    int64_t tile_seq[2];               // sequence whose rows a tile holds (-1 = none)
-    int2 copy_list[kProdWarps][32];    // per producer warp: (kv row, slot) of the rows to copy
-    float colred[4][kHeads];           // per-warp column max of the current tile
-    float m[kHeads];                   // running max (log2 units)
-    alignas(16) float mu[kHeads];      // the running max with -inf replaced by 0
-    float alpha[kHeads];               // rescale factor of this tile
+    int need_corr[3];                  // per tile, in rotation: some head raised its maximum
+    alignas(8) uint16_t vmask16[2][4];  // claimed slots of the tile in each kv buffer, 16 a piece
+    uint32_t ring_bits[3][4];          // per pair, in rotation: residues mod 128 of valid rows
+    int ring_count[3];                 // number of valid rows of a pair
+    int64_t pair_seq[3];               // sequence whose rows a pair holds
+    int row_id[2 * kRows];             // kv row held by each slot of the two buffers, -1 = none
+    int2 copy_list[kProdWarps][2][32];  // per producer warp and tile: (kv row, slot) to copy
+    float alpha[2][kHeads];            // rescale factor of the tile, per tile parity
     float stats_m[2][kHeads];          // final max (0 when none) per task parity
+    float stats_l[2][kHeads];          // final sum per task parity
     alignas(16) float inv[4][kHeads];  // epilogue: 1 / denominator, a table per epilogue warp
-    float sink[128];                   // the sinks of every head
-    alignas(16) uint8_t fp8_sc[kRows][16];  // e8m0 scales of the rows an fp8 tile widens, by slot
+    float sink[kHeads];                // the sinks of the CTA's head block
+    alignas(16) uint8_t fp8_sc[2 * kRows][16];  // e8m0 scales of the rows an fp8 tile widens
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
+    const __nv_bfloat16* q;    // for the L2 prefetch of the next task's rows
     const __nv_bfloat16* kv;   // bf16 rows (bf16 kv)
     const uint8_t* kv8;        // e4m3 rows and their e8m0 scales (fp8 kv)
     const uint8_t* kv_scale;
@@ -123,8 +129,8 @@ struct Params {
     int topk;
     int n_tiles;
     int n_splits;
-    int tiles_per_split;
-    int64_t n_units;  // (token, split) units; each is one task per head block
+    int tiles_per_split;  // even when the columns are split, so that pairs never straddle tasks
+    int64_t n_units;      // (token, split) units; each is one task per head block
 };
 
 struct Task {
@@ -185,6 +191,13 @@ __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v));
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -203,6 +216,13 @@ __device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t& phase, volatile 
     return ok;
 }
 
+// Byte offset, inside the kv buffers, of 16-byte unit u (of 64) of the row in slot ps (bit 6 =
+// the buffer, bits 0-5 = the row of the tile): block u / 8 of the buffer, 128-byte swizzle.
+__device__ __forceinline__ uint32_t kv_unit_off(int ps, int u) {
+    return (uint32_t)(ps >> 6) * kBufBytes + (uint32_t)(u >> 3) * kBlkBytes + (uint32_t)(ps & 63) * 128 +
+           ((((uint32_t)u & 7) ^ ((uint32_t)ps & 7)) << 4);
+}
+
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap o_map,
@@ -216,29 +236,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_p = smem_addr(smem + kOffP);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &M.abort;
+    const int hb = (int)(blockIdx.x % p.hblocks);
 
     if (tid == 0) {
         mbar_init(smem_addr(&M.q_full), 1);
         mbar_init(smem_addr(&M.q_empty), 1);
-        for (int c = 0; c < kGroups; ++c) {
-            mbar_init(smem_addr(&M.kv_full[c]), kProdThreads);
-            mbar_init(smem_addr(&M.kv_empty[c]), 1);
-        }
         for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&M.kv_full[b]), kProdThreads);
+            mbar_init(smem_addr(&M.kv_empty[b]), 1);
             mbar_init(smem_addr(&M.s_full[b]), 1);
             mbar_init(smem_addr(&M.s_empty[b]), 128);
-            mbar_init(smem_addr(&M.stats_full[b]), 1);
+            mbar_init(smem_addr(&M.p_full[b]), 128);
+            mbar_init(smem_addr(&M.p_empty[b]), 1);
+            mbar_init(smem_addr(&M.stats_full[b]), 128);
+            mbar_init(smem_addr(&M.stats_empty[b]), 128);
         }
-        mbar_init(smem_addr(&M.p_full), 128);
-        mbar_init(smem_addr(&M.p_empty), 1);
         mbar_init(smem_addr(&M.o_full), 1);
-        for (int c = 0; c < kGroups; ++c) mbar_init(smem_addr(&M.o_empty[c]), 128);
+        for (int c = 0; c < kChunks; ++c) mbar_init(smem_addr(&M.o_empty[c]), 128);
         mbar_init(smem_addr(&M.sm_bar), 128);
-        mbar_init(smem_addr(&M.ep_bar), 128);
         mbar_init(smem_addr(&M.pr_bar), kProdThreads);
         mbar_init(smem_addr(&M.done), 1);
         M.abort = 0;
-        M.need_corr[0] = M.need_corr[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -246,14 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     // every slot starts as a finite (zero) row that no tile claims
-    for (int i = tid; i < 2 * kRows; i += kThreads) (&M.row_id[0][0])[i] = -1;
-    if (tid < 8) (&M.ring_bits[0][0])[tid] = 0;
-    if (tid < 2) {
+    for (int i = tid; i < 2 * kRows; i += kThreads) M.row_id[i] = -1;
+    if (tid < 12) (&M.ring_bits[0][0])[tid] = 0;
+    if (tid < 3) {
         M.ring_count[tid] = 0;
-        M.tile_seq[tid] = -1;
+        M.pair_seq[tid] = -1;
+        M.need_corr[tid] = 0;
     }
-    for (int i = tid; i < p.h; i += kThreads) M.sink[i] = p.sink[i];
-    for (uint32_t i = tid; i < kKvBytes / 16; i += kThreads)
+    for (int i = tid; i < kHeads; i += kThreads)
+        M.sink[i] = hb * kHeads + i < p.h ? p.sink[hb * kHeads + i] : 0.f;
+    for (uint32_t i = tid; i < 2 * kBufBytes / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + kOffKv)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1 && lane == 0) tma_prefetch_desc(&q_map);
@@ -262,106 +282,145 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = M.tmem_base;
-    if (warp >= kWarpSoftmax && warp < kWarpEpilogue) {  // all-ones bf16 A operand for the row sums
-        tmem_st_32x32b_x8(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kColOnes, 0x3F803F80u);
-        tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     int64_t tb, te;
     task_range(p, tb, te);
-
 
     if (warp == 0) {
         // ------------------------------------------------------------------ MMA issue
         // The whole warp runs this loop (descriptors stay in uniform registers); each MMA and
         // commit is issued by one elected lane, and every lane waits on the barriers.  A wait's
         // result is made warp-uniform so that a time-out cannot split the warp.
-        {
-            constexpr uint32_t id_s = idesc_bf16_f32(kRows, kHeads, false, false);
-            constexpr uint32_t id_o = idesc_bf16_f32(kRows, kHeads, true, true);
-            constexpr uint32_t id_l = idesc_bf16_f32(kRows, kHeads, false, true);
-            // base descriptors; the per-instruction ones add a start-address offset (>> 4)
-            const uint64_t a_s0 = smem_desc_sw128(s_kv, 16, 1024);
-            const uint64_t b_s0 = smem_desc_sw128(s_q, 16, 1024);
-            const uint64_t a_o0 = smem_desc_sw128(s_kv, 16384, 1024);
-            const uint64_t b_o0 = smem_desc_sw128(s_p, 8192, 1024);
-            uint32_t T = 0;
-            int64_t k = 0;
-            bool ok = true;
-            Task t = task_of(p, tb);
-            for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
-                const uint32_t kp = (uint32_t)(k & 1);
-                if (t.t0 == t.t1) {  // nothing listed for this task: keep every phase in step
-                    ok = warp_wait(smem_addr(&M.q_full), kp, abort);
-                    mma_commit_elect(smem_addr(&M.q_empty));
-                    for (int c = 0; c < kGroups && ok; ++c)
-                        ok = warp_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort);
-                    mma_commit_elect(smem_addr(&M.o_full));
-                    continue;
-                }
-                for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
-                    const uint32_t b = T & 1, use = (T >> 1) & 1, tp = T & 1;
-                    const uint32_t s_col = tmem + kColS + 64 * b;
-                    // S^T = KV . Q^T: every wait first, then the 32 MMAs back to back
-                    ok = warp_wait(smem_addr(&M.s_empty[b]), use ^ 1, abort);
-                    if (ok && ti == t.t0) ok = warp_wait(smem_addr(&M.q_full), kp, abort);
-                    if (!ok) break;
-                    // K step ks (16 of 512): block ks / 4 of the tile / Q, 32 B per step inside
-                    // a 128-byte row (2 in the descriptor's 16-byte address units); each 128-d
-                    // chunk of the tile as soon as it has landed (the chunk loop is kept rolled: the
-                    // issuing warp shares its instruction cache with three other roles)
+        constexpr uint32_t id_s = idesc_bf16_f32(kHeads, kRows, false, false);
+        constexpr uint32_t id_o = idesc_bf16_f32(128, kHeads, true, false);
+        // base descriptors; the per-instruction ones add a start-address offset (>> 4)
+        const uint64_t a_s0 = smem_desc_sw128(s_q, 16, 1024);          // Q, K-major
+        const uint64_t b_s0 = smem_desc_sw128(s_kv, 16, 1024);         // tile rows, K-major
+        const uint64_t a_o0 = smem_desc_sw128(s_kv, kBlkBytes, 1024);  // tile^T, MN-major
+        const uint64_t b_o0 = smem_desc_sw128(s_p, 16, 1024);          // P, K-major
+        // O^T += KV^T . P^T for tile pt (pt & 1 = its kv and P buffer) of task kk
+        auto issue_pv = [&](uint32_t pt, bool first, bool last, int64_t kk) -> bool {
+            const uint32_t b = pt & 1;
+            if (!warp_wait(smem_addr(&M.p_full[b]), (pt >> 1) & 1, abort)) return false;
+            tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < kGroups; ++c) {
-                        if (!(ok = warp_wait(smem_addr(&M.kv_full[c]), tp, abort))) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int ks = 8 * c; ks < 8 * c + 8; ++ks)
-                            mma_bf16_ss_elect(s_col, a_s0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
-                                        b_s0 + (uint64_t)((ks >> 2) * 512 + (ks & 3) * 2), id_s,
-                                        ks != 0);
-                    }
-                    if (!ok) break;
-                    if (ti == t.t1 - 1) mma_commit_elect(smem_addr(&M.q_empty));
-                    mma_commit_elect(smem_addr(&M.s_full[b]));
-                    // O^T += KV^T . P^T
-                    ok = warp_wait(smem_addr(&M.p_full), tp, abort);
-                    if (!ok) break;
+            for (int c = 0; c < kChunks; ++c) {
+                if (first) {  // the epilogue has read this chunk of the last task's O
+                    if (!warp_wait(smem_addr(&M.o_empty[c]), (uint32_t)(kk & 1) ^ 1, abort)) return false;
                     tc_fence_after();
+                }
+                // K step ks = rows 16 ks .. 16 ks + 15 (2 KB of the two 64-d blocks of chunk c)
+#pragma unroll
+                for (int ks = 0; ks < kRows / 16; ++ks)
+                    mma_bf16_ss_elect(tmem + kColO + 64 * c,
+                                      a_o0 + (uint64_t)(b * (kBufBytes >> 4) + c * (2 * kBlkBytes >> 4) +
+                                                        ks * (16 * 128 >> 4)),
+                                      b_o0 + (uint64_t)(b * (kPBytes >> 4) + ks * 2), id_o,
+                                      !(first && ks == 0));
+            }
+            mma_commit_elect(smem_addr(&M.kv_empty[b]));  // the tile's rows are read
+            mma_commit_elect(smem_addr(&M.p_empty[b]));
+            if (last) mma_commit_elect(smem_addr(&M.o_full));
+            return true;
+        };
+        bool ok = true;
+        if (p.n_tiles == 0) {
+            // every task is empty (no idx columns): keep every phase in step
+            int64_t k = 0;
+            for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
+                const uint32_t kp = (uint32_t)(k & 1);
+                ok = warp_wait(smem_addr(&M.q_full), kp, abort);
+                mma_commit_elect(smem_addr(&M.q_empty));
+                for (int c = 0; c < kChunks && ok; ++c)
+                    ok = warp_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort);
+                mma_commit_elect(smem_addr(&M.o_full));
+            }
+        } else {
+            // Two cursors over the CTA's tiles (every task has at least one): the next logits
+            // and the next P.V.  Whichever is ready is issued, the P.V first (it releases a kv
+            // buffer to the gather); the logits of a tile can so run during the softmax of the
+            // one before.  Readiness is polled without blocking; the poll is bounded.
+            struct Cursor {
+                Task t;
+                int64_t tau, k;
+                int ti;
+                uint32_t T;
+            };
+            auto advance = [&](Cursor& c) {
+                ++c.T;
+                if (++c.ti == c.t.t1) {
+                    ++c.tau;
+                    ++c.k;
+                    task_step(p, c.t);
+                    c.ti = c.t.t0;
+                }
+            };
+            Cursor cs;
+            cs.t = task_of(p, tb);
+            cs.tau = tb;
+            cs.k = 0;
+            cs.ti = cs.t.t0;
+            cs.T = 0;
+            Cursor cv = cs;
+            uint32_t idle = 0;
+            while (cv.tau < te) {
+                bool did = false;
+                if (cv.T < cs.T &&
+                    __all_sync(0xffffffffu, mbar_test_wait(smem_addr(&M.p_full[cv.T & 1]), (cv.T >> 1) & 1))) {
+                    if (!(ok = issue_pv(cv.T, cv.ti == cv.t.t0, cv.ti == cv.t.t1 - 1, cv.k))) break;
+                    advance(cv);
+                    did = true;
+                } else if (cs.tau < te) {
+                    const uint32_t b = cs.T & 1, use = cs.T >> 1;
+                    const bool first = cs.ti == cs.t.t0;
+                    const bool rdy = mbar_test_wait(smem_addr(&M.s_empty[b]), (use & 1) ^ 1) &&
+                                     mbar_test_wait(smem_addr(&M.kv_full[b]), use & 1) &&
+                                     (!first || mbar_test_wait(smem_addr(&M.q_full), (uint32_t)(cs.k & 1)));
+                    if (__all_sync(0xffffffffu, rdy)) {
+                        tc_fence_after();
+                        // S = Q . tile^T: K step 4 kb + kq (16 of 512) = block kb of Q and of the
+                        // tile, 32 B per step inside a 128-byte row (the block loop is kept rolled:
+                        // the issuing warp shares its instruction cache with three other roles)
 #pragma unroll 1
-                    for (int c = 0; c < kGroups; ++c) {
-                        if (ti == t.t0) {  // the epilogue has read this chunk of the last task's O
-                            if (!(ok = warp_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort))) break;
-                            tc_fence_after();
+                        for (int kb = 0; kb < 8; ++kb) {
+#pragma unroll
+                            for (int kq = 0; kq < 4; ++kq)
+                                mma_bf16_ss_elect(tmem + kColS + 64 * b,
+                                                  a_s0 + (uint64_t)(kb * (kBlkBytes >> 4) + kq * 2),
+                                                  b_s0 + (uint64_t)(b * (kBufBytes >> 4) + kb * (kBlkBytes >> 4) + kq * 2),
+                                                  id_s, (kb | kq) != 0);
                         }
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks)  // 16 rows = 2 KB per K step
-                            mma_bf16_ss_elect(tmem + kColO + 64 * c, a_o0 + (uint64_t)(c * 2048 + ks * 128),
-                                        b_o0 + (uint64_t)(ks * 128), id_o, !(ti == t.t0 && ks == 0));
-                        mma_commit_elect(smem_addr(&M.kv_empty[c]));  // chunk c of the tile is read
+                        if (cs.ti == cs.t.t1 - 1) mma_commit_elect(smem_addr(&M.q_empty));
+                        mma_commit_elect(smem_addr(&M.s_full[b]));
+                        advance(cs);
+                        did = true;
                     }
-                    if (!ok) break;
-                    // l += ones . P^T (every element of the A operand is 1, so one 8-column
-                    // block of TMEM serves every K step)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ts_elect(tmem + kColSum, tmem + kColOnes, b_o0 + (uint64_t)(ks * 128),
-                                    id_l, !(ti == t.t0 && ks == 0));
-                    mma_commit_elect(smem_addr(&M.p_empty));
-                    if (ti == t.t1 - 1) mma_commit_elect(smem_addr(&M.o_full));
+                }
+                if (did) {
+                    idle = 0;
+                } else {
+                    if (__any_sync(0xffffffffu, *abort != 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (++idle > (1u << 22)) {  // nothing became ready for a very long time
+                        *abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    if (idle > 64) __nanosleep(32);
                 }
             }
-            // let every issued MMA finish before the accumulators are released
-            mma_commit_elect(smem_addr(&M.done));
-            warp_wait(smem_addr(&M.done), 0, abort);
         }
+        // let every issued MMA finish before the accumulators are released
+        mma_commit_elect(smem_addr(&M.done));
+        warp_wait(smem_addr(&M.done), 0, abort);
     } else if (warp == 1) {
         // ------------------------------------------------------------------ Q loads (TMA)
         if (lane == 0) {
             int64_t k = 0;
             bool ok = true;
             Task t = task_of(p, tb);
+            const int hc = min(kHeads, p.h - hb * kHeads);
             for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
                 const int32_t y = (int32_t)(t.token * p.h + (int64_t)t.hb * kHeads);
                 ok = mbar_wait(smem_addr(&M.q_empty), (uint32_t)(k & 1) ^ 1, abort);
@@ -371,6 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c)  // 8 boxes of [64 heads x 64 d], 128-byte swizzle
                     tma_load_2d(s_q + c * 8192, &q_map, 64 * c, y, bar);
+                // the next task's rows (when it is another token) into L2 meanwhile
+                if (tau + 1 < te && t.split == p.n_splits - 1) {
+                    const __nv_bfloat16* qn = p.q + ((t.token + 1) * p.h + (int64_t)hb * kHeads) * kD;
+#pragma unroll 1
+                    for (int i = 0; i < hc; i += 8)
+                        prefetch_l2(qn + (int64_t)i * kD, (uint32_t)(min(8, hc - i) * kD * 2));
+                }
             }
             // after a failed wait, let the last Q load land before the CTA exits
             if (!ok && k > 0) mbar_drain(smem_addr(&M.q_full), (uint32_t)((k - 1) & 1));
@@ -378,65 +444,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < kWarpSoftmax) {
         // ------------------------------------------------------------------ kv gather
-        // Each thread resolves one of the tile's 128 slots; every warp lists the rows it copies
-        // and copies each 128-d chunk of them (cp.async, one commit group per chunk) as soon as
-        // the previous tile's P.V has finished reading that chunk; chunk c is signalled once the
-        // group has landed.
-        const int pw = warp - 2;       // producer warp 0 .. kProdWarps - 1
-        const int pt_id = tid - 64;    // the tile slot (column placement) this thread resolves
-        uint32_t T = 0, pr_phase = 0;
+        // Each thread resolves one of the 128 columns of a pair of tiles; every warp lists the
+        // rows it copies into each of the pair's tiles, and copies a tile's rows (cp.async, one
+        // commit group) as soon as the P.V two tiles back has released that kv buffer.  Warp w
+        // resolves columns 16 w .. 16 w + 15 of each tile (lanes 0-15 the first tile, 16-31 the
+        // second), so that every warp has rows to copy into both tiles.
+        const int pw = warp - 2;  // producer warp 0 .. kProdWarps - 1
+        const int pt = (lane >> 4) * kRows + 16 * pw + (lane & 15);  // its pair column (and slot)
+        uint32_t T = 0, pr_phase = 0, g3 = 0;
         bool ok = true;
         Task t = task_of(p, tb);
         for (int64_t tau = tb; tau < te && ok; ++tau, task_step(p, t)) {
             const int64_t bi = t.seq;
             const int32_t* idx_tok = p.idx + t.token * (int64_t)p.topk;
-            const __nv_bfloat16* kvb = p.kv + bi * p.rows * (int64_t)kD;
-            for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
-                const uint32_t tp = T & 1;
-                const int col = ti * kRows + pt_id;
-                int j = col < p.topk ? __ldg(idx_tok + col) : -1;
+            const int colend = min(p.topk, t.t1 * kRows);
+            for (int ti = t.t0; ti < t.t1 && ok; ti += 2) {
+                const int nt = min(2, t.t1 - ti);  // tiles of this pair
+                const uint32_t gprev = g3 == 0 ? 2 : g3 - 1, gnext = g3 == 2 ? 0 : g3 + 1;
+                const int col = ti * kRows + pt;
+                int j = col < colend ? __ldg(idx_tok + col) : -1;
                 if (j < -1 || j >= p.rows) {
                     atomicOr(p.status, kStatusBadIndex);
                     j = -1;
                 }
-                // placement: ring (slot = j mod 128) when the valid rows' residues are distinct.
-                // (row_id[tp] is only written after the tile barrier below: the softmax of the
-                // tile two back, which has the same parity, may still be reading it until then.)
+                // ring placement (slot = j mod 128) when the valid rows' residues are distinct
+                // (the per-pair records rotate over three entries: the one for the pair after
+                // this is cleared after this pair's barrier, and is next written after the
+                // next pair's barrier)
                 if (j >= 0) {
-                    atomicOr(&M.ring_bits[tp][(j & 127) >> 5], 1u << (j & 31));
-                    atomicAdd(&M.ring_count[tp], 1);
+                    atomicOr(&M.ring_bits[g3][(j & 127) >> 5], 1u << (j & 31));
+                    atomicAdd(&M.ring_count[g3], 1);
                 }
-                if (pt_id == 0) M.tile_seq[tp] = bi;
+                if (pt == 0) M.pair_seq[g3] = bi;
                 if (!(ok = wg_sync(smem_addr(&M.pr_bar), pr_phase, abort))) break;
                 // a slot's row can be kept only if it belongs to this same sequence
-                const bool same_seq = M.tile_seq[tp ^ 1] == bi;
-                const bool ring = __popc(M.ring_bits[tp][0]) + __popc(M.ring_bits[tp][1]) +
-                                      __popc(M.ring_bits[tp][2]) + __popc(M.ring_bits[tp][3]) ==
-                                  M.ring_count[tp];
+                const bool same_seq = M.pair_seq[gprev] == bi;
+                const bool ring = nt == 2 &&
+                                  __popc(M.ring_bits[g3][0]) + __popc(M.ring_bits[g3][1]) +
+                                          __popc(M.ring_bits[g3][2]) + __popc(M.ring_bits[g3][3]) ==
+                                      M.ring_count[g3];
                 // this thread's own slot is empty unless a row claims it
-                const bool claimed = ring ? ((M.ring_bits[tp][pt_id >> 5] >> (pt_id & 31)) & 1) != 0
-                                          : j >= 0;
-                if (!claimed) M.row_id[tp][pt_id] = -1;
-                const int slot = ring ? (j & 127) : pt_id;
-                const bool copy = j >= 0 && (!same_seq || M.row_id[tp ^ 1][slot] != j);
-                if (j >= 0) M.row_id[tp][slot] = j;
-                if (pt_id == 0) {  // the next tile (other parity) starts from a clean slate
-                    M.ring_bits[tp ^ 1][0] = M.ring_bits[tp ^ 1][1] = 0;
-                    M.ring_bits[tp ^ 1][2] = M.ring_bits[tp ^ 1][3] = 0;
-                    M.ring_count[tp ^ 1] = 0;
+                const bool claimed = ring ? ((M.ring_bits[g3][pt >> 5] >> (pt & 31)) & 1) != 0 : j >= 0;
+                const int slot = ring ? (j & 127) : pt;
+                // slot s of the pair is row s % 64 of the kv buffer of tile T + s / 64 (every
+                // slot of both buffers is rewritten, so a one-tile pair forgets the other buffer)
+                const int ps_own = (int)((((T + (uint32_t)(pt >> 6)) & 1) << 6) | (uint32_t)(pt & 63));
+                const int ps = (int)((((T + (uint32_t)(slot >> 6)) & 1) << 6) | (uint32_t)(slot & 63));
+                if (!claimed) M.row_id[ps_own] = -1;
+                const bool copy = j >= 0 && !(same_seq && M.row_id[ps] == j);
+                if (j >= 0) M.row_id[ps] = j;
+                if (pt == 0) {
+                    M.ring_bits[gnext][0] = M.ring_bits[gnext][1] = 0;
+                    M.ring_bits[gnext][2] = M.ring_bits[gnext][3] = 0;
+                    M.ring_count[gnext] = 0;
                 }
-                // the rows this warp copies, compacted into a list (ballot prefix count)
-                const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, copy);
-                const int ncopy = __popc(m0);
-                if (copy) M.copy_list[pw][__popc(m0 & ((1u << lane) - 1u))] = make_int2(j, slot);
-                // the previous tile is usually still in use: pull this tile's new rows into L2
-                // now, so that the copies issued once its chunks are released hit L2
+                g3 = gnext;
+                // the claimed slots (16 of each tile: slots 16 pw .. 16 pw + 15 in the first
+                // tile's half of the ballot, the second tile's in the other) and the rows it copies
+                // into each tile, compacted into lists (ballot prefix counts)
+                const uint32_t m_claim = __ballot_sync(0xFFFFFFFFu, claimed);
+                const int half = slot >> 6;
+                const uint32_t mh0 = __ballot_sync(0xFFFFFFFFu, copy && half == 0);
+                const uint32_t mh1 = __ballot_sync(0xFFFFFFFFu, copy && half == 1);
                 if (copy) {
+                    const uint32_t mh = half ? mh1 : mh0;
+                    M.copy_list[pw][half][__popc(mh & ((1u << lane) - 1u))] = make_int2(j, ps);
+                    // the buffers are usually still in use: pull the new rows into L2 now, so
+                    // that the copies issued once a buffer is released hit L2
                     if constexpr (kFp8) {
                         prefetch_l2(p.kv8 + (bi * p.rows + j) * (int64_t)kD, kD);
                         prefetch_l2(p.kv_scale + (bi * p.rows + j) * (int64_t)(kD / 32), kD / 32);
                     } else {
-                        prefetch_l2(kvb + (int64_t)j * kD, kD * 2);
+                        prefetch_l2(p.kv + (bi * p.rows + j) * (int64_t)kD, kD * 2);
                     }
                 }
                 __syncwarp();
@@ -448,285 +527,245 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint8_t* kvb8 = p.kv8 + bi * p.rows * (int64_t)kD;
                     const uint8_t* scb = p.kv_scale + bi * p.rows * (int64_t)(kD / 32);
                     const int unit = lane & 7;
-                    int2 ent8[8];
+#pragma unroll 1
+                    for (int hx = 0; hx < nt && ok; ++hx) {
+                        const uint32_t Tx = T + hx, b = Tx & 1;
+                        const int ncopy = __popc(hx ? mh1 : mh0);
+                        int2 ent8[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int e = (lane >> 3) + 4 * i;
-                        ent8[i] = e < ncopy ? M.copy_list[pw][e] : make_int2(-1, 0);
-                    }
-                    // stage every chunk as soon as P.V has released it ...
+                        for (int i = 0; i < 8; ++i) {
+                            const int e = (lane >> 3) + 4 * i;
+                            ent8[i] = e < ncopy ? M.copy_list[pw][hx][e] : make_int2(-1, 0);
+                        }
+                        if (!(ok = mbar_wait(smem_addr(&M.kv_empty[b]), ((Tx >> 1) & 1) ^ 1, abort))) break;
+                        M.vmask16[b][pw] = (uint16_t)(hx ? m_claim >> 16 : m_claim);
+                        if (lane < ncopy) {  // the row's 16 scales
+                            const int2 en = M.copy_list[pw][hx][lane];
+                            cp_async16(smem_addr(&M.fp8_sc[en.y][0]), scb + (int64_t)en.x * (kD / 32), 16u);
+                        }
+                        // stage every chunk ...
 #pragma unroll
-                    for (int c = 0; c < kGroups; ++c) {
-                        if (ok) ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
-                        if (ok) {
-                            if (c == 0 && lane < ncopy) {  // the row's 16 scales
-                                const int2 en = M.copy_list[pw][lane];
-                                cp_async16(smem_addr(&M.fp8_sc[en.y][0]),
-                                           scb + (int64_t)en.x * (kD / 32), 16u);
-                            }
+                        for (int c = 0; c < 4; ++c) {
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
                                 if (ent8[i].x < 0) break;
-                                cp_async16(s_kv + (2 * c + 1) * 16384 + ent8[i].y * 128 + unit * 16,
+                                const int r = ent8[i].y;
+                                cp_async16(s_kv + (uint32_t)(r >> 6) * kBufBytes + (2 * c + 1) * kBlkBytes +
+                                               (uint32_t)(r & 63) * 128 + unit * 16,
                                            kvb8 + (int64_t)ent8[i].x * kD + 128 * c + unit * 16, 16u);
+                            }
+                            cp_async_commit();
+                        }
+                        // ... then widen them in order, each once its group has landed
+#pragma unroll
+                        for (int cw = 0; cw < 4; ++cw) {
+                            if (cw == 0) cp_async_wait<3>();
+                            else if (cw == 1) cp_async_wait<2>();
+                            else if (cw == 2) cp_async_wait<1>();
+                            else cp_async_wait<0>();
+                            __syncwarp();  // every lane's staged codes are visible to the warp
+                            uint4 code[8];
+                            float sc[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                if (ent8[i].x < 0) break;
+                                const int r = ent8[i].y;
+                                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(code[i].x), "=r"(code[i].y), "=r"(code[i].z), "=r"(code[i].w)
+                                             : "r"(s_kv + (uint32_t)(r >> 6) * kBufBytes + (2 * cw + 1) * kBlkBytes +
+                                                   (uint32_t)(r & 63) * 128 + unit * 16)
+                                             : "memory");
+                                sc[i] = fp8::e8m0_to_f32(M.fp8_sc[r][4 * cw + (unit >> 1)]);
+                            }
+                            __syncwarp();  // all codes read before any lane overwrites them
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                if (ent8[i].x < 0) break;
+                                const int r = ent8[i].y;
+                                uint4 lo, hi;
+                                fp8::dequant16(code[i], sc[i], lo, hi);
+                                const int u = 16 * cw + 2 * unit;  // 16-byte bf16 units u, u + 1
+                                st_shared_v4(s_kv + kv_unit_off(r, u), lo.x, lo.y, lo.z, lo.w);
+                                st_shared_v4(s_kv + kv_unit_off(r, u + 1), hi.x, hi.y, hi.z, hi.w);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(smem_addr(&M.kv_full[b]));
+                    }
+                    T += nt;
+                    continue;
+                }
+                const __nv_bfloat16* kvb = p.kv + bi * p.rows * (int64_t)kD;
+                // a tile with at most two new rows (e.g. the next token of a sliding window):
+                // load them into registers now, while the buffers are still in use; lane l
+                // holds 16-byte units l and 32 + l of a row
+                uint4 v[2][2][2];
+                int2 ent_r[2][2];
+#pragma unroll
+                for (int hx = 0; hx < 2; ++hx) {
+                    const int n = __popc(hx ? mh1 : mh0);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        ent_r[hx][e] = (hx < nt && n <= 2 && e < n) ? M.copy_list[pw][hx][e] : make_int2(-1, 0);
+                        if (ent_r[hx][e].x >= 0) {
+                            const uint4* src = reinterpret_cast<const uint4*>(kvb + (int64_t)ent_r[hx][e].x * kD);
+                            v[hx][e][0] = __ldg(src + lane);
+                            v[hx][e][1] = __ldg(src + 32 + lane);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int hx = 0; hx < 2; ++hx) {
+                    if (hx >= nt || !ok) break;
+                    const uint32_t Tx = T + hx, b = Tx & 1;
+                    const int ncopy = __popc(hx ? mh1 : mh0);
+                    if (!(ok = mbar_wait(smem_addr(&M.kv_empty[b]), ((Tx >> 1) & 1) ^ 1, abort))) break;
+                    M.vmask16[b][pw] = (uint16_t)(hx ? m_claim >> 16 : m_claim);
+                    if (ncopy <= 2) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            if (ent_r[hx][e].x < 0) continue;
+                            const int r = ent_r[hx][e].y;
+                            const uint4 w0 = v[hx][e][0], w1 = v[hx][e][1];
+                            st_shared_v4(s_kv + kv_unit_off(r, lane), w0.x, w0.y, w0.z, w0.w);
+                            st_shared_v4(s_kv + kv_unit_off(r, 32 + lane), w1.x, w1.y, w1.z, w1.w);
+                        }
+                    } else {
+                        // entries e0 + lane / 16 + 2 i (two rows per instruction); 16-byte unit
+                        // lane % 16 of each 256-byte quarter of the row
+#pragma unroll 1
+                        for (int e0 = 0; e0 < ncopy; e0 += 8) {
+                            int2 ent[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int e = e0 + (lane >> 4) + 2 * i;
+                                ent[i] = e < ncopy ? M.copy_list[pw][hx][e] : make_int2(-1, 0);
+                            }
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const int u = 16 * c + (lane & 15);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    if (ent[i].x < 0) break;
+                                    cp_async16(s_kv + kv_unit_off(ent[i].y, u),
+                                               kvb + (int64_t)ent[i].x * kD + u * 8, 16u);
+                                }
                             }
                         }
                         cp_async_commit();
+                        cp_async_wait<0>();
                     }
-                    // ... then widen them in order, each once its group has landed
-#pragma unroll
-                    for (int cw = 0; cw < kGroups; ++cw) {
-                        if (cw == 0) cp_async_wait<3>();
-                        else if (cw == 1) cp_async_wait<2>();
-                        else if (cw == 2) cp_async_wait<1>();
-                        else cp_async_wait<0>();
-                        __syncwarp();  // every lane's staged codes are visible to the warp
-                        uint4 code[8];
-                        float sc[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            if (ent8[i].x < 0) break;
-                            const int r = ent8[i].y;
-                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                         : "=r"(code[i].x), "=r"(code[i].y), "=r"(code[i].z), "=r"(code[i].w)
-                                         : "r"(s_kv + (2 * cw + 1) * 16384 + r * 128 + unit * 16)
-                                         : "memory");
-                            sc[i] = fp8::e8m0_to_f32(M.fp8_sc[r][4 * cw + (unit >> 1)]);
-                        }
-                        __syncwarp();  // all codes read before any lane overwrites them
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            if (ent8[i].x < 0) break;
-                            const int r = ent8[i].y;
-                            uint4 lo, hi;
-                            fp8::dequant16(code[i], sc[i], lo, hi);
-                            const int u = 16 * cw + 2 * unit;  // 16-byte bf16 units u, u + 1
-                            const uint32_t row = s_kv + (u >> 3) * 16384 + r * 128;
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                             row + ((((u & 7) ^ (r & 7)) & 7) << 4)),
-                                         "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w)
-                                         : "memory");
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                             row + (((((u + 1) & 7) ^ (r & 7)) & 7) << 4)),
-                                         "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
-                                         : "memory");
-                        }
-                        fence_proxy_async_smem();
-                        mbar_arrive(smem_addr(&M.kv_full[cw]));
-                    }
-                    if (!ok) break;
-                    continue;
+                    fence_proxy_async_smem();
+                    mbar_arrive(smem_addr(&M.kv_full[b]));
                 }
-                if (ncopy <= 2) {
-                    // few new rows (e.g. the next token of a sliding window): load them into
-                    // registers now, while the previous tile is still being used, and write them
-                    // to their slots chunk by chunk as the tile is released
-                    uint4 v[2][2];
-                    int2 ent[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        ent[e] = e < ncopy ? M.copy_list[pw][e] : make_int2(-1, 0);
-                        if (ent[e].x >= 0) {
-                            const uint4* src = reinterpret_cast<const uint4*>(kvb + (int64_t)ent[e].x * kD);
-                            v[e][0] = __ldg(src + lane);
-                            v[e][1] = __ldg(src + 32 + lane);
-                        }
-                    }
-                    // chunk c (units 16 c .. 16 c + 15) is held by the lanes with lane / 16 ==
-                    // c % 2, in v[.][c / 2]; each chunk is written and signalled as soon as P.V
-                    // has released it
-#pragma unroll
-                    for (int c = 0; c < kGroups; ++c) {
-                        if (ok) ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
-                        if (ok && (lane >> 4) == (c & 1)) {
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                if (ent[e].x < 0) continue;
-                                const int r = ent[e].y;
-                                const int u = 32 * (c >> 1) + lane;  // 16-byte unit of the 1 KB row
-                                const uint4 w = v[e][c >> 1];
-                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                                 s_kv + (u >> 3) * 16384 + r * 128 +
-                                                 ((((u & 7) ^ (r & 7)) & 7) << 4)),
-                                             "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
-                                             : "memory");
-                            }
-                        }
-                        fence_proxy_async_smem();
-                        mbar_arrive(smem_addr(&M.kv_full[c]));
-                    }
-                    if (!ok) break;
-                    continue;
-                }
-                // this lane's rows of the list: entries lane / 16 + 2 i (two rows per instruction)
-                int2 ent[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int e = (lane >> 4) + 2 * i;
-                    ent[i] = e < ncopy ? M.copy_list[pw][e] : make_int2(-1, 0);
-                }
-                // chunk c = 16-byte units 16 c .. 16 c + 15 of each row (blocks 2 c and 2 c + 1)
-#pragma unroll
-                for (int c = 0; c < kGroups; ++c) {
-                    if (ok) ok = mbar_wait(smem_addr(&M.kv_empty[c]), tp ^ 1, abort);
-                    if (ok) {
-                        const int u = 16 * c + (lane & 15);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (ent[i].x < 0) break;
-                            const int r = ent[i].y;
-                            const uint32_t dst =
-                                s_kv + (u >> 3) * 16384 + r * 128 + ((((u & 7) ^ (r & 7)) & 7) << 4);
-                            cp_async16(dst, kvb + (int64_t)ent[i].x * kD + u * 8, 16u);
-                        }
-                    }
-                    cp_async_commit();  // (an empty group after a failed wait keeps the count)
-                }
-                if (!ok) break;
-                cp_async_wait<3>();
-                fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&M.kv_full[0]));
-                cp_async_wait<2>();
-                fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&M.kv_full[1]));
-                cp_async_wait<1>();
-                fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&M.kv_full[2]));
-                cp_async_wait<0>();
-                fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&M.kv_full[3]));
+                T += nt;
             }
         }
         cp_async_wait<0>();
     } else if (warp < kWarpEpilogue) {
         // ------------------------------------------------------------------ softmax
-        // Per tile: column max of the logits -> running max m (raised only past the threshold),
-        // p = 2^(x - m) written as P^T, and the tile's column sums; the sums are folded into the
-        // running l = alpha * l + sum at the next tile (and once more at the end of the task).
+        // Per tile: the head's maximum over the tile -> running max m (raised only past the
+        // threshold), p = 2^(x - m) written as the head's P row, and the running sum
+        // l = alpha l + sum p; O is rescaled (rarely) before the tile's P.V.
         const int q4 = warp & 3;
-        const int row = 32 * q4 + lane;  // TMEM lane = tile row
+        const int hf = lane >> 4;                // which 32 of the tile's 64 columns
+        const int hh = 16 * q4 + (lane & 15);    // the head (within the block) of this thread
+        const int st = tid - 32 * kWarpSoftmax;  // 0 .. 127
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        uint32_t T = 0, sm_phase = 0;
+        uint32_t T = 0, sm_phase = 0, c3 = 0;
         int64_t k = 0;
         bool ok = true;
         Task t = task_of(p, tb);
         for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
             const int kpar = (int)(k & 1);
+            float m = -INFINITY, mu = 0.f, l = 0.f;
             for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
-                const uint32_t b = T & 1, use = (T >> 1) & 1, tp = T & 1;
+                const uint32_t b = T & 1, use = T >> 1;
                 const bool first = ti == t.t0;
-                ok = mbar_wait(smem_addr(&M.kv_full[0]), tp, abort);  // the tile's row ids
-                if (ok) ok = mbar_wait(smem_addr(&M.s_full[b]), use, abort);
+                ok = mbar_wait(smem_addr(&M.kv_full[b]), use & 1, abort);  // the tile's slot set
+                if (ok) ok = mbar_wait(smem_addr(&M.s_full[b]), use & 1, abort);
                 if (!ok) break;
-                // an empty slot's logits become -inf (pass 1) and its P^T row zeros (pass 2)
-                const bool valid = M.row_id[tp][row] >= 0;
-                const float row_bias = valid ? 0.f : -INFINITY;
-                const uint32_t row_mask = valid ? 0xFFFFFFFFu : 0u;
-                const uint32_t s_addr = tmem + lane_base + kColS + 64 * b;
                 tc_fence_after();
-                // pass 1: column maximum of the scaled logits over the 128 rows; lane i keeps the
-                // warp maxima of heads i and 32 + i
-                {
-                    uint32_t r[kHeads];
-                    tmem_ld_32x32b_x64(s_addr, r);
-                    tmem_wait_ld();
-                    float mine0 = -INFINITY, mine1 = -INFINITY;
+                uint32_t r[32];
+                tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kColS + 64 * b, r);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(smem_addr(&M.s_empty[b]));
+                // scaled logits (log2 units); an unclaimed slot's become -inf
+                const uint32_t vm = reinterpret_cast<const uint32_t*>(M.vmask16[b])[hf];
+                float x[32];
+                float mt = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < kHeads; ++i) {
-                        const float x = fmaf(__uint_as_float(r[i]), p.scale_log2, row_bias);
-                        float mx;
-                        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(x));
-                        if (i < 32) {
-                            if (lane == i) mine0 = mx;
-                        } else {
-                            if (lane == i - 32) mine1 = mx;
-                        }
-                    }
-                    M.colred[q4][lane] = mine0;
-                    M.colred[q4][32 + lane] = mine1;
+                for (int i = 0; i < 32; ++i) {
+                    x[i] = ((vm >> i) & 1u) ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                    mt = fmaxf(mt, x[i]);
                 }
-                if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
-                if (row < kHeads) {
-                    const int h = row;
-                    const float cm = fmaxf(fmaxf(M.colred[0][h], M.colred[1][h]),
-                                           fmaxf(M.colred[2][h], M.colred[3][h]));
-                    const float mo = M.m[h];
-                    float mn, al = 1.f;
-                    if (first) {
-                        mn = cm;
-                    } else {
-                        mn = cm > mo + kRescaleThreshold ? cm : mo;
-                        if (mn != mo) {
-                            al = fast_exp2(mo - mn);  // 0 when mo = -inf (nothing summed yet)
-                            M.need_corr[tp] = 1;
-                        }
-                    }
-                    M.m[h] = mn;
-                    M.mu[h] = mn == -INFINITY ? 0.f : mn;
-                    M.alpha[h] = al;
+                mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
+                float al = 1.f, mn = mt;
+                if (!first) {
+                    mn = mt > m + kRescaleThreshold ? mt : m;
+                    if (mn != m) al = fast_exp2(m - mn);  // 0 when m = -inf (nothing summed yet)
                 }
+                if (hf == 0) {
+                    M.alpha[b][hh] = al;
+                    if (!first && mn != m) M.need_corr[c3] = 1;
+                }
+                m = mn;
+                mu = mn == -INFINITY ? 0.f : mn;
+                // p = 2^(x - m): this thread's 32 columns are 16-byte units 4 hf .. 4 hf + 3 of
+                // the head's 128-byte P row (swizzled like every K-major operand)
+                uint32_t pk[16];
+                float ps = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float e0 = fast_exp2(x[2 * i] - mu), e1 = fast_exp2(x[2 * i + 1] - mu);
+                    ps += e0 + e1;
+                    pk[i] = pack_bf16(e0, e1);
+                }
+                l = first ? ps : fmaf(al, l, ps);
+                // the P buffer is free once the P.V two tiles back has completed
+                if (!(ok = mbar_wait(smem_addr(&M.p_empty[b]), (use & 1) ^ 1, abort))) break;
+                const uint32_t prow = s_p + b * kPBytes + (uint32_t)hh * 128;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    st_shared_v4(prow + ((((uint32_t)(4 * hf + u)) ^ ((uint32_t)hh & 7)) << 4), pk[4 * u],
+                                 pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
-                const bool corr = !first && M.need_corr[tp];
-                if (row == 0) M.need_corr[tp ^ 1] = 0;
-
-                // P buffer free and the previous PV done (O stable)
-                ok = mbar_wait(smem_addr(&M.p_empty), tp ^ 1, abort);
-                if (!ok) break;
+                const bool corr = !first && M.need_corr[c3] != 0;
+                // (clear the entry of the tile after next: its writers are past the next barrier)
+                if (st == 0) M.need_corr[c3 == 0 ? 2 : c3 - 1] = 0;
+                c3 = c3 == 2 ? 0 : c3 + 1;
                 if (corr) {
+                    // O must hold the previous tile's P.V before it is rescaled
+                    const uint32_t pb = (T - 1) & 1;
+                    if (!(ok = mbar_wait(smem_addr(&M.p_empty[pb]), ((T - 1) >> 1) & 1, abort))) break;
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < 2 * kGroups + 2; ++c) {  // O^T (8 blocks), then l (2)
-                        uint32_t r[32];
-                        const uint32_t ta = tmem + lane_base +
-                                            (c < 2 * kGroups ? kColO + 32 * c : kColSum + 32 * (c & 1));
-                        tmem_ld_32x32b_x32(ta, r);
+                    for (int c = 0; c < 2 * kChunks; ++c) {  // O^T in 8 blocks of 32 heads
+                        uint32_t o[32];
+                        const uint32_t ta = tmem + lane_base + kColO + 32 * c;
+                        tmem_ld_32x32b_x32(ta, o);
                         tmem_wait_ld();
-                        const float* al = &M.alpha[32 * (c & 1)];
+                        const float* alc = &M.alpha[b][32 * (c & 1)];
 #pragma unroll
-                        for (int h = 0; h < 32; ++h)
-                            r[h] = __float_as_uint(__uint_as_float(r[h]) * al[h]);
-                        tmem_st_32x32b_x32(ta, r);
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alc[i]);
+                        tmem_st_32x32b_x32(ta, o);
                     }
                     tmem_wait_st();
                 }
-                // pass 2: p = 2^(x - m) as the P^T row (128-byte swizzled MN-major operand); the
-                // sums are accumulated by the tensor core from P^T
-                {
-                    uint32_t r[kHeads];
-                    tmem_ld_32x32b_x64(s_addr, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {  // 16-byte unit u of the row: heads 8u .. 8u + 7
-                        const float4 ma = *reinterpret_cast<const float4*>(&M.mu[8 * u]);
-                        const float4 mb = *reinterpret_cast<const float4*>(&M.mu[8 * u + 4]);
-                        const float mu8[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-                        float e[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            e[i] = fast_exp2(fmaf(__uint_as_float(r[8 * u + i]), p.scale_log2, -mu8[i]));
-                        const uint32_t dst = s_p + row * 128 + (((u ^ (row & 7)) & 7) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                                     "r"(pack_bf16(e[0], e[1]) & row_mask),
-                                     "r"(pack_bf16(e[2], e[3]) & row_mask),
-                                     "r"(pack_bf16(e[4], e[5]) & row_mask),
-                                     "r"(pack_bf16(e[6], e[7]) & row_mask));
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(smem_addr(&M.s_empty[b]));
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(smem_addr(&M.p_full));
+                mbar_arrive(smem_addr(&M.p_full[b]));
             }
             if (!ok) break;
-            // final statistics of the task: the running max per head (the sums are in TMEM)
-            if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
-            if (row < kHeads) {
-                const float mh = t.t1 > t.t0 ? M.m[row] : -INFINITY;
-                M.stats_m[kpar][row] = mh == -INFINITY ? 0.f : mh;
+            // the task's statistics, once the epilogue has read those of two tasks back
+            if (!(ok = mbar_wait(smem_addr(&M.stats_empty[kpar]), (uint32_t)((k >> 1) & 1) ^ 1, abort))) break;
+            l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+            if (hf == 0) {
+                M.stats_m[kpar][hh] = t.t1 > t.t0 ? mu : 0.f;
+                M.stats_l[kpar][hh] = t.t1 > t.t0 ? l : 0.f;
             }
-            if (!(ok = wg_sync(smem_addr(&M.sm_bar), sm_phase, abort))) break;
-            if (row == 0) mbar_arrive(smem_addr(&M.stats_full[kpar]));
+            mbar_arrive(smem_addr(&M.stats_full[kpar]));
         }
     } else {
         // ------------------------------------------------------------------ epilogue
@@ -736,7 +775,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with itself.  Every thread passes every barrier of a task, even after a failed wait, so
         // the warpgroup's barriers never split.
         const int q4 = warp & 3;
-        const int et = tid - 32 * kWarpEpilogue;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         // this warp's box: 32 rows (heads) of 64 bytes (32 d); this thread's word in a row holds
         // the d pair 2 (lane / 2), 2 (lane / 2) + 1
@@ -756,45 +794,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool split = p.n_splits > 1;
             const int64_t pbase = (t.token * p.n_splits + t.split) * (int64_t)p.h + h0;
-            // the denominators: every TMEM lane of the sum block holds the same row sums, so
-            // each warp reads them all and lane l finishes heads l and l + 32 into the warp's own
-            // table (no barrier across the warps)
-            {
-                float lsum[2];
+            // the denominators: lane l finishes heads l and l + 32 into the warp's own table
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + kColSum + 32 * hh, r);
-                    tmem_wait_ld();
-                    float v = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (lane == i) v = __uint_as_float(r[i]);
-                    lsum[hh] = t.t1 > t.t0 ? v : 0.f;
-                }
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int h = lane + 32 * hh;
-                    const float l = lsum[hh], mu = M.stats_m[kpar][h];
-                    float inv = 0.f;
-                    if (ok && h < hc) {
-                        if (split) {
-                            if (q4 == 0) {
-                                p.part_ml[(pbase + h) * 2 + 0] = mu;
-                                p.part_ml[(pbase + h) * 2 + 1] = l;
-                            }
-                        } else if (l > 0.f) {
-                            inv = 1.f / (l + fast_exp2(M.sink[h0 + h] * kLog2e - mu));
+            for (int hq = 0; hq < 2; ++hq) {
+                const int h = lane + 32 * hq;
+                const float l = M.stats_l[kpar][h], mu = M.stats_m[kpar][h];
+                float inv = 0.f;
+                if (ok && h < hc) {
+                    if (split) {
+                        if (q4 == 0) {
+                            p.part_ml[(pbase + h) * 2 + 0] = mu;
+                            p.part_ml[(pbase + h) * 2 + 1] = l;
                         }
+                    } else if (l > 0.f) {
+                        inv = 1.f / (l + fast_exp2(M.sink[h] * kLog2e - mu));
                     }
-                    M.inv[q4][h] = inv;
                 }
-                __syncwarp();
+                M.inv[q4][h] = inv;
             }
+            mbar_arrive(smem_addr(&M.stats_empty[kpar]));
+            __syncwarp();
 #pragma unroll 1
-            for (int c = 0; c < kGroups; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
                 uint32_t r[kHeads];
-                tmem_ld_32x32b_x64(tmem + lane_base + 64 * c, r);
+                tmem_ld_32x32b_x64(tmem + lane_base + kColO + 64 * c, r);
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(smem_addr(&M.o_empty[c]));  // the MMA may refill this chunk now
@@ -816,21 +839,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // so a head with inv = 0 comes out as zeros.)
                     uint32_t out[16];
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        const float4 w = *reinterpret_cast<const float4*>(&M.inv[q4][32 * rh + 4 * m]);
-                        const int a = 32 * rh + 4 * m;
+                    for (int mq = 0; mq < 8; ++mq) {
+                        const float4 w = *reinterpret_cast<const float4*>(&M.inv[q4][32 * rh + 4 * mq]);
+                        const int a = 32 * rh + 4 * mq;
                         const uint32_t pk0 = pack_bf16(__uint_as_float(r[a]) * w.x,
                                                        __uint_as_float(r[a + 1]) * w.y);
                         const uint32_t pk1 = pack_bf16(__uint_as_float(r[a + 2]) * w.z,
                                                        __uint_as_float(r[a + 3]) * w.w);
-                        out[2 * m] = __byte_perm(pk0, __shfl_xor_sync(0xffffffffu, pk0, 1), sel);
-                        out[2 * m + 1] = __byte_perm(pk1, __shfl_xor_sync(0xffffffffu, pk1, 1), sel);
+                        out[2 * mq] = __byte_perm(pk0, __shfl_xor_sync(0xffffffffu, pk0, 1), sel);
+                        out[2 * mq + 1] = __byte_perm(pk1, __shfl_xor_sync(0xffffffffu, pk1, 1), sel);
                     }
                     // the box is free once this warp's previous store has read it
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) st_shared_b32(st_base + 128 * j, out[j]);
+                    for (int jj = 0; jj < 16; ++jj) st_shared_b32(st_base + 128 * jj, out[jj]);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && ok && h0 + 32 * rh < p.h) {
@@ -887,21 +910,28 @@ struct TcGeometry {
 };
 
 // Split the idx columns of a token over several tasks only when the tokens alone cannot fill
-// the GPU (decode); the split count is device-independent so the workspace size is too.
+// the GPU (decode), at pair-of-tiles boundaries; the split count is device-independent so the
+// workspace size is too.
 TcGeometry tc_geometry(int64_t n_tokens, int h, int topk) {
     constexpr int kAssumedSms = 152;
     TcGeometry g;
     g.n_tiles = (topk + kRows - 1) / kRows;
     g.hblocks = (h + kHeads - 1) / kHeads;
+    const int pairs = (g.n_tiles + 1) / 2;
     const int64_t base = n_tokens * g.hblocks;
     int splits = 1;
-    if (g.n_tiles > 1 && base < kAssumedSms) {
+    if (pairs > 1 && base < kAssumedSms) {
         splits = (int)(kAssumedSms / base);
-        if (splits > g.n_tiles) splits = g.n_tiles;
+        if (splits > pairs) splits = pairs;
         if (splits < 1) splits = 1;
     }
-    g.tiles_per_split = splits > 1 ? (g.n_tiles + splits - 1) / splits : (g.n_tiles > 0 ? g.n_tiles : 1);
-    g.n_splits = splits > 1 ? (g.n_tiles + g.tiles_per_split - 1) / g.tiles_per_split : 1;
+    if (splits > 1) {
+        g.tiles_per_split = 2 * ((pairs + splits - 1) / splits);
+        g.n_splits = (g.n_tiles + g.tiles_per_split - 1) / g.tiles_per_split;
+    } else {
+        g.tiles_per_split = g.n_tiles > 0 ? g.n_tiles : 1;
+        g.n_splits = 1;
+    }
     return g;
 }
 
@@ -950,6 +980,7 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
 
     Params p;
     const bool fp8 = c.kv_format == SA_KV_FP8_E4M3;
+    p.q = reinterpret_cast<const __nv_bfloat16*>(c.q);
     p.kv = fp8 ? nullptr : reinterpret_cast<const __nv_bfloat16*>(c.kv);
     p.kv8 = fp8 ? reinterpret_cast<const uint8_t*>(c.kv) : nullptr;
     p.kv_scale = fp8 ? c.kv_scale : nullptr;
