@@ -527,23 +527,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint8_t* kvb8 = p.kv8 + bi * p.rows * (int64_t)kD;
                     const uint8_t* scb = p.kv_scale + bi * p.rows * (int64_t)(kD / 32);
                     const int unit = lane & 7;
-#pragma unroll 1
-                    for (int hx = 0; hx < nt && ok; ++hx) {
-                        const uint32_t Tx = T + hx, b = Tx & 1;
+                    // stage each tile as soon as its buffer is released (one commit group per
+                    // tile), then widen them in order: the first tile's widening overlaps the
+                    // second's copies
+                    // (a tile's list entries (lane / 8) + 4 i are read from the list where needed)
+                    auto load_ent = [&](int hx, int2 (&ent)[8]) {
                         const int ncopy = __popc(hx ? mh1 : mh0);
-                        int2 ent8[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int e = (lane >> 3) + 4 * i;
-                            ent8[i] = e < ncopy ? M.copy_list[pw][hx][e] : make_int2(-1, 0);
+                            ent[i] = e < ncopy ? M.copy_list[pw][hx][e] : make_int2(-1, 0);
                         }
+                    };
+#pragma unroll
+                    for (int hx = 0; hx < 2; ++hx) {
+                        if (hx >= nt || !ok) break;
+                        const uint32_t Tx = T + hx, b = Tx & 1;
+                        const int ncopy = __popc(hx ? mh1 : mh0);
+                        int2 ent8[8];
+                        load_ent(hx, ent8);
                         if (!(ok = mbar_wait(smem_addr(&M.kv_empty[b]), ((Tx >> 1) & 1) ^ 1, abort))) break;
                         M.vmask16[b][pw] = (uint16_t)(hx ? m_claim >> 16 : m_claim);
                         if (lane < ncopy) {  // the row's 16 scales
                             const int2 en = M.copy_list[pw][hx][lane];
                             cp_async16(smem_addr(&M.fp8_sc[en.y][0]), scb + (int64_t)en.x * (kD / 32), 16u);
                         }
-                        // stage every chunk ...
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -554,16 +562,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                (uint32_t)(r & 63) * 128 + unit * 16,
                                            kvb8 + (int64_t)ent8[i].x * kD + 128 * c + unit * 16, 16u);
                             }
-                            cp_async_commit();
                         }
-                        // ... then widen them in order, each once its group has landed
+                        cp_async_commit();
+                    }
 #pragma unroll
+                    for (int hx = 0; hx < 2; ++hx) {
+                        if (hx >= nt || !ok) break;
+                        const uint32_t b = (T + hx) & 1;
+                        if (hx == 0 && nt == 2) cp_async_wait<1>();
+                        else cp_async_wait<0>();
+                        __syncwarp();  // every lane's staged codes are visible to the warp
+                        int2 ent8[8];
+                        load_ent(hx, ent8);
+#pragma unroll 1
                         for (int cw = 0; cw < 4; ++cw) {
-                            if (cw == 0) cp_async_wait<3>();
-                            else if (cw == 1) cp_async_wait<2>();
-                            else if (cw == 2) cp_async_wait<1>();
-                            else cp_async_wait<0>();
-                            __syncwarp();  // every lane's staged codes are visible to the warp
                             uint4 code[8];
                             float sc[8];
 #pragma unroll
