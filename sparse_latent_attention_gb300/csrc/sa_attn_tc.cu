@@ -20,9 +20,10 @@
 // o = O / (l + 2^(sink log2e - m)).
 //
 // Roles (persistent CTAs, one 64-head block of one query token per task, 448 threads):
-//   warp 0      MMA issue (one elected lane) and TMEM allocation; the P.V of a tile is issued
-//               before the logits of the next, so that the gather of a buffer overlaps the
-//               softmax and P.V of the other
+//   warp 0      MMA issue (one elected lane) and TMEM allocation; the next logits and the next
+//               P.V are each issued as soon as they are ready (the P.V first when both are), so
+//               the gather of one buffer, the logits of its tile and the softmax and P.V of the
+//               other tile overlap
 //   warp 1      Q loads (TMA, 128-byte swizzle) and an L2 prefetch of the next task's Q
 //   warps 2-5   kv row gather: the 128 idx columns of a pair of tiles at a time, one per thread;
 //               cp.async 16 B into the swizzled layout (fp8 rows are staged raw and widened in
@@ -71,12 +72,15 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kColO = 0, kColS = 256;
 
 // Shared-memory map (dynamic, 1024-byte aligned base)
-constexpr uint32_t kBlkBytes = kRows * 128;       // 8 KB: [64 rows x 64 d] with 128-byte rows
-constexpr uint32_t kBufBytes = 8 * kBlkBytes;     // 64 KB: one tile, 8 blocks of 64 d
+// The two kv buffers are interleaved by 64-d block: [8 blocks of 64 d][buffer][64 rows][128 B]
+constexpr uint32_t kBlkBytes = kRows * 128;       // 8 KB: one buffer's [64 rows x 64 d]
+constexpr uint32_t kDBlkBytes = 2 * kBlkBytes;    // 16 KB: a 64-d block of both buffers
+constexpr uint32_t kKvBytes = 8 * kDBlkBytes;     // 128 KB
+constexpr uint32_t kQBlkBytes = kHeads * 128;     // 8 KB: [64 heads x 64 d] of Q
 constexpr uint32_t kQBytes = kHeads * kD * 2;     // 64 KB: 8 blocks of [64 heads x 128 B]
 constexpr uint32_t kPBytes = kHeads * kRows * 2;  // 8 KB: [64 heads x 128 B] per P buffer
 constexpr uint32_t kOffKv = 0;
-constexpr uint32_t kOffQ = kOffKv + 2 * kBufBytes;
+constexpr uint32_t kOffQ = kOffKv + kKvBytes;
 constexpr uint32_t kOffP = kOffQ + kQBytes;
 // o staging: one [32 heads x 32 d] box of 64-byte rows (no swizzle) per epilogue warp
 constexpr uint32_t kStageBoxBytes = 32 * 64;
@@ -217,9 +221,9 @@ __device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t& phase, volatile 
 }
 
 // Byte offset, inside the kv buffers, of 16-byte unit u (of 64) of the row in slot ps (bit 6 =
-// the buffer, bits 0-5 = the row of the tile): block u / 8 of the buffer, 128-byte swizzle.
+// the buffer, bits 0-5 = the row of the tile): 64-d block u / 8, 128-byte swizzle.
 __device__ __forceinline__ uint32_t kv_unit_off(int ps, int u) {
-    return (uint32_t)(ps >> 6) * kBufBytes + (uint32_t)(u >> 3) * kBlkBytes + (uint32_t)(ps & 63) * 128 +
+    return (uint32_t)(u >> 3) * kDBlkBytes + (uint32_t)(ps >> 6) * kBlkBytes + (uint32_t)(ps & 63) * 128 +
            ((((uint32_t)u & 7) ^ ((uint32_t)ps & 7)) << 4);
 }
 
@@ -273,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = tid; i < kHeads; i += kThreads)
         M.sink[i] = hb * kHeads + i < p.h ? p.sink[hb * kHeads + i] : 0.f;
-    for (uint32_t i = tid; i < 2 * kBufBytes / 16; i += kThreads)
+    for (uint32_t i = tid; i < kKvBytes / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + kOffKv)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1 && lane == 0) tma_prefetch_desc(&q_map);
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // base descriptors; the per-instruction ones add a start-address offset (>> 4)
         const uint64_t a_s0 = smem_desc_sw128(s_q, 16, 1024);          // Q, K-major
         const uint64_t b_s0 = smem_desc_sw128(s_kv, 16, 1024);         // tile rows, K-major
-        const uint64_t a_o0 = smem_desc_sw128(s_kv, kBlkBytes, 1024);  // tile^T, MN-major
+        const uint64_t a_o0 = smem_desc_sw128(s_kv, kDBlkBytes, 1024);  // tile^T, MN-major
         const uint64_t b_o0 = smem_desc_sw128(s_p, 16, 1024);          // P, K-major
         // O^T += KV^T . P^T for tile pt (pt & 1 = its kv and P buffer) of task kk
         auto issue_pv = [&](uint32_t pt, bool first, bool last, int64_t kk) -> bool {
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < kRows / 16; ++ks)
                     mma_bf16_ss_elect(tmem + kColO + 64 * c,
-                                      a_o0 + (uint64_t)(b * (kBufBytes >> 4) + c * (2 * kBlkBytes >> 4) +
+                                      a_o0 + (uint64_t)(b * (kBlkBytes >> 4) + c * (2 * kDBlkBytes >> 4) +
                                                         ks * (16 * 128 >> 4)),
                                       b_o0 + (uint64_t)(b * (kPBytes >> 4) + ks * 2), id_o,
                                       !(first && ks == 0));
@@ -380,14 +384,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // S = Q . tile^T: K step 4 kb + kq (16 of 512) = block kb of Q and of the
                         // tile, 32 B per step inside a 128-byte row (the block loop is kept rolled:
                         // the issuing warp shares its instruction cache with three other roles)
+                        const uint32_t s_col = tmem + kColS + 64 * b;
+                        const uint64_t b_sb = b_s0 + (uint64_t)(b * (kBlkBytes >> 4));
 #pragma unroll 1
                         for (int kb = 0; kb < 8; ++kb) {
 #pragma unroll
                             for (int kq = 0; kq < 4; ++kq)
-                                mma_bf16_ss_elect(tmem + kColS + 64 * b,
-                                                  a_s0 + (uint64_t)(kb * (kBlkBytes >> 4) + kq * 2),
-                                                  b_s0 + (uint64_t)(b * (kBufBytes >> 4) + kb * (kBlkBytes >> 4) + kq * 2),
-                                                  id_s, (kb | kq) != 0);
+                                mma_bf16_ss_elect(s_col, a_s0 + (uint64_t)(kb * (kQBlkBytes >> 4) + kq * 2),
+                                                  b_sb + (uint64_t)(kb * (kDBlkBytes >> 4) + kq * 2), id_s,
+                                                  (kb | kq) != 0);
                         }
                         if (cs.ti == cs.t.t1 - 1) mma_commit_elect(smem_addr(&M.q_empty));
                         mma_commit_elect(smem_addr(&M.s_full[b]));
@@ -558,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int i = 0; i < 8; ++i) {
                                 if (ent8[i].x < 0) break;
                                 const int r = ent8[i].y;
-                                cp_async16(s_kv + (uint32_t)(r >> 6) * kBufBytes + (2 * c + 1) * kBlkBytes +
+                                cp_async16(s_kv + (2 * c + 1) * kDBlkBytes + (uint32_t)(r >> 6) * kBlkBytes +
                                                (uint32_t)(r & 63) * 128 + unit * 16,
                                            kvb8 + (int64_t)ent8[i].x * kD + 128 * c + unit * 16, 16u);
                             }
@@ -584,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const int r = ent8[i].y;
                                 asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                                              : "=r"(code[i].x), "=r"(code[i].y), "=r"(code[i].z), "=r"(code[i].w)
-                                             : "r"(s_kv + (uint32_t)(r >> 6) * kBufBytes + (2 * cw + 1) * kBlkBytes +
+                                             : "r"(s_kv + (2 * cw + 1) * kDBlkBytes + (uint32_t)(r >> 6) * kBlkBytes +
                                                    (uint32_t)(r & 63) * 128 + unit * 16)
                                              : "memory");
                                 sc[i] = fp8::e8m0_to_f32(M.fp8_sc[r][4 * cw + (unit >> 1)]);
