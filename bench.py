@@ -49,9 +49,9 @@ L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 # from the ncu captures summarised under profiles/, keyed by (hash of the CUDA sources the capture
 # ran, workload).  Any change to the sources makes the key miss, so a stale figure reads as null.
 NCU_TRAFFIC = {
-    ("88a28cbac99e2795", "swa_prefill"): 501_384_704,
-    ("88a28cbac99e2795", "cmp_prefill"): 1_068_094_976,
-    ("88a28cbac99e2795", "decode"): 83_754_496,
+    ("6f457e81f12d8228", "swa_prefill"): 500_314_624,
+    ("6f457e81f12d8228", "cmp_prefill"): 1_065_895_936,
+    ("6f457e81f12d8228", "decode"): 83_265_280,
 }
 
 
