@@ -217,6 +217,35 @@ def test_random_parity(dev, case):
     assert (_gpu.bf16_tensor_to_u16(o.view(-1, h, d)[1]) == 0).all()
 
 
+def test_running_max_raised_every_tile(dev):
+    # The logits grow by ~7 nats (> 2^8 in log2 units) from one block of 64 rows to the next, so
+    # a token that lists the rows in order raises its running maximum (and rescales O) on every
+    # row tile; the reversed order never does, and a shuffled order with holes does sometimes.
+    rng = np.random.default_rng(2024)
+    b, s, h, d, rows = 1, 3, 64, 512, 704
+    scale = d ** -0.5
+    q0 = rng.standard_normal(d)
+    q = q0[None, None, None, :] + 0.1 * rng.standard_normal((b, s, h, d))
+    kv = 0.5 * rng.standard_normal((b, rows, d))
+    kv += (np.arange(rows) // 64)[None, :, None] * 7.0 * (q0 / np.linalg.norm(q0))[None, None, :]
+    q_bits, kv_bits = oracle.bf16_round(q), oracle.bf16_round(kv)
+    sink = rng.standard_normal(h).astype(np.float32)
+    idx = np.empty((b, s, rows), dtype=np.int32)
+    idx[0, 0] = np.arange(rows)
+    idx[0, 1] = np.arange(rows)[::-1]
+    perm = rng.permutation(rows).astype(np.int32)
+    perm[rng.random(rows) < 0.2] = -1
+    idx[0, 2] = perm
+    ws = sa.new_workspace(b, s, h, d, rows, rows, device=dev)
+    o = sa.sparse_attn(_gpu.u16_to_bf16_tensor(q_bits, dev), _gpu.u16_to_bf16_tensor(kv_bits, dev),
+                       torch.from_numpy(sink).to(dev), torch.from_numpy(idx).to(dev), scale,
+                       workspace=ws)
+    torch.cuda.synchronize()
+    assert sa.read_status(ws) == 0
+    want = oracle.sparse_attn(q_bits, kv_bits, sink, idx, scale)
+    assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what="growing logits")
+
+
 def test_sink_minus_inf_and_single_row(dev):
     wl = workloads.make_random(2, 5, 64, 512, 40, 24, seed=77, neg_frac=0.0)
     wl.sink[:] = -np.inf
