@@ -90,6 +90,7 @@ constexpr uint32_t kOffMisc = kOffStage + 4 * kStageBoxBytes;
 struct Misc {
     uint64_t q_full, q_empty;
     uint64_t kv_full[2], kv_empty[2];  // per kv buffer
+    uint64_t staged[2];                // fp8: a tile's raw codes have landed (per kv buffer)
     uint64_t s_full[2], s_empty[2];    // per S buffer (TMEM)
     uint64_t p_full[2], p_empty[2];    // per P buffer (shared memory)
     uint64_t o_full, o_empty[kChunks];
@@ -104,6 +105,7 @@ struct Misc {
     int64_t pair_seq[3];               // sequence whose rows a pair holds
     int row_id[2 * kRows];             // kv row held by each slot of the two buffers, -1 = none
     int2 copy_list[kProdWarps][2][32];  // per producer warp and tile: (kv row, slot) to copy
+    int copy_n[kProdWarps][2];          // the lengths of those lists
     float alpha[2][kHeads];            // rescale factor of the tile, per tile parity
     float stats_m[2][kHeads];          // final max (0 when none) per task parity
     float stats_l[2][kHeads];          // final sum per task parity
@@ -227,6 +229,47 @@ __device__ __forceinline__ uint32_t kv_unit_off(int ps, int u) {
            ((((uint32_t)u & 7) ^ ((uint32_t)ps & 7)) << 4);
 }
 
+// Widens 128-d chunks c0 .. c1 - 1 of the fp8 rows a warp lists, in place: the e4m3 codes of chunk
+// c sit raw in 64-d block 2c + 1 of the row's slot and become bf16 in blocks 2c and 2c + 1 (exact:
+// see sa_fp8.cuh).  Lane l moves 16-code unit l % 8 (`unit`) of list entries l / 8 + 4 i (ent[i],
+// x < 0 = none); the row's 16 e8m0 scales are in fp8_sc.
+__device__ __forceinline__ void widen_fp8(uint32_t s_kv, const Misc& M, const int2 (&ent)[8], int unit,
+                                          int c0, int c1) {
+#pragma unroll 1
+    for (int cw = c0; cw < c1; ++cw) {
+        // entries in two groups of four; a row's 8 lanes read all its codes before any writes
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            uint4 code[4];
+            float sc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int2 en = ent[4 * g + i];
+                if (en.x < 0) break;
+                const int r = en.y;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(code[i].x), "=r"(code[i].y), "=r"(code[i].z), "=r"(code[i].w)
+                             : "r"(s_kv + (2 * cw + 1) * kDBlkBytes + (uint32_t)(r >> 6) * kBlkBytes +
+                                   (uint32_t)(r & 63) * 128 + unit * 16)
+                             : "memory");
+                sc[i] = fp8::e8m0_to_f32(M.fp8_sc[r][4 * cw + (unit >> 1)]);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int2 en = ent[4 * g + i];
+                if (en.x < 0) break;
+                const int r = en.y;
+                uint4 lo, hi;
+                fp8::dequant16(code[i], sc[i], lo, hi);
+                const int u = 16 * cw + 2 * unit;  // 16-byte bf16 units u, u + 1
+                st_shared_v4(s_kv + kv_unit_off(r, u), lo.x, lo.y, lo.z, lo.w);
+                st_shared_v4(s_kv + kv_unit_off(r, u + 1), hi.x, hi.y, hi.z, hi.w);
+            }
+        }
+    }
+}
+
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap o_map,
@@ -246,7 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&M.q_full), 1);
         mbar_init(smem_addr(&M.q_empty), 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_addr(&M.kv_full[b]), kProdThreads);
+            // fp8: the epilogue warps widen half of every tile, so they arrive too
+            mbar_init(smem_addr(&M.kv_full[b]), kFp8 ? kProdThreads + 128 : kProdThreads);
+            mbar_init(smem_addr(&M.staged[b]), kProdThreads);
             mbar_init(smem_addr(&M.kv_empty[b]), 1);
             mbar_init(smem_addr(&M.s_full[b]), 1);
             mbar_init(smem_addr(&M.s_empty[b]), 128);
@@ -511,6 +556,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int half = slot >> 6;
                 const uint32_t mh0 = __ballot_sync(0xFFFFFFFFu, copy && half == 0);
                 const uint32_t mh1 = __ballot_sync(0xFFFFFFFFu, copy && half == 1);
+                if constexpr (kFp8) {
+                    // the epilogue warps read the previous pair's lists until they have widened
+                    // its tiles (their arrival completes a tile's kv_full)
+                    if (T > 0 && !(ok = mbar_wait(smem_addr(&M.kv_full[(T - 1) & 1]), ((T - 1) >> 1) & 1, abort)))
+                        break;
+                    if (T > 1 && !(ok = mbar_wait(smem_addr(&M.kv_full[(T - 2) & 1]), ((T - 2) >> 1) & 1, abort)))
+                        break;
+                    if (lane == 0) {
+                        M.copy_n[pw][0] = __popc(mh0);
+                        M.copy_n[pw][1] = __popc(mh1);
+                    }
+                }
                 if (copy) {
                     const uint32_t mh = half ? mh1 : mh0;
                     M.copy_list[pw][half][__popc(mh & ((1u << lane) - 1u))] = make_int2(j, ps);
@@ -577,35 +634,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (hx == 0 && nt == 2) cp_async_wait<1>();
                         else cp_async_wait<0>();
                         __syncwarp();  // every lane's staged codes are visible to the warp
+                        // the epilogue warps widen chunks 2 and 3 of the tile, this warp 0 and 1
+                        mbar_arrive(smem_addr(&M.staged[b]));
                         int2 ent8[8];
                         load_ent(hx, ent8);
-#pragma unroll 1
-                        for (int cw = 0; cw < 4; ++cw) {
-                            uint4 code[8];
-                            float sc[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                if (ent8[i].x < 0) break;
-                                const int r = ent8[i].y;
-                                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                             : "=r"(code[i].x), "=r"(code[i].y), "=r"(code[i].z), "=r"(code[i].w)
-                                             : "r"(s_kv + (2 * cw + 1) * kDBlkBytes + (uint32_t)(r >> 6) * kBlkBytes +
-                                                   (uint32_t)(r & 63) * 128 + unit * 16)
-                                             : "memory");
-                                sc[i] = fp8::e8m0_to_f32(M.fp8_sc[r][4 * cw + (unit >> 1)]);
-                            }
-                            __syncwarp();  // all codes read before any lane overwrites them
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                if (ent8[i].x < 0) break;
-                                const int r = ent8[i].y;
-                                uint4 lo, hi;
-                                fp8::dequant16(code[i], sc[i], lo, hi);
-                                const int u = 16 * cw + 2 * unit;  // 16-byte bf16 units u, u + 1
-                                st_shared_v4(s_kv + kv_unit_off(r, u), lo.x, lo.y, lo.z, lo.w);
-                                st_shared_v4(s_kv + kv_unit_off(r, u + 1), hi.x, hi.y, hi.z, hi.w);
-                            }
-                        }
+                        widen_fp8(s_kv, M, ent8, unit, 0, 2);
                         fence_proxy_async_smem();
                         mbar_arrive(smem_addr(&M.kv_full[b]));
                     }
@@ -802,11 +835,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t k = 0;
         bool ok = true;
         Task t = task_of(p, tb);
+        // fp8: the next tile whose chunks 2 and 3 this warpgroup widens (warp q4 takes the rows
+        // producer warp q4 listed)
+        int64_t wtau = p.n_tiles > 0 ? tb : te;
+        int wsplit = t.split, wt0 = t.t0, wt1 = t.t1, wti = t.t0;
+        uint32_t wT = 0;
         for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
             const int kpar = (int)(k & 1);
             const int h0 = t.hb * kHeads;
             const int hc = min(kHeads, p.h - h0);
-            ok = mbar_wait(smem_addr(&M.o_full), (uint32_t)kpar, abort);
+            if constexpr (kFp8) {
+                // widen every tile the producers have staged until this task's O is complete
+                // (its last tile needs this warpgroup's widening first); the poll is bounded
+                uint32_t idle = 0;
+                while (true) {
+                    if (wtau < te &&
+                        __all_sync(0xffffffffu, mbar_test_wait(smem_addr(&M.staged[wT & 1]), (wT >> 1) & 1))) {
+                        const int hx = (wti - wt0) & 1;
+                        const int ncopy = M.copy_n[q4][hx];
+                        int2 ent8[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int e = (lane >> 3) + 4 * i;
+                            ent8[i] = e < ncopy ? M.copy_list[q4][hx][e] : make_int2(-1, 0);
+                        }
+                        widen_fp8(s_kv, M, ent8, lane & 7, 2, 4);
+                        fence_proxy_async_smem();
+                        mbar_arrive(smem_addr(&M.kv_full[wT & 1]));
+                        ++wT;
+                        if (++wti == wt1) {  // the next unit's tiles (splits fastest, as task_step)
+                            ++wtau;
+                            if (++wsplit == p.n_splits) wsplit = 0;
+                            wt0 = wsplit * p.tiles_per_split;
+                            wt1 = min(p.n_tiles, wt0 + p.tiles_per_split);
+                            wti = wt0;
+                        }
+                        idle = 0;
+                        continue;
+                    }
+                    if (__all_sync(0xffffffffu, mbar_test_wait(smem_addr(&M.o_full), (uint32_t)kpar))) break;
+                    if (__any_sync(0xffffffffu, *abort != 0) || ++idle > (1u << 22)) {
+                        *abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    if (idle > 64) __nanosleep(32);
+                }
+            }
+            ok = ok && mbar_wait(smem_addr(&M.o_full), (uint32_t)kpar, abort);
             if (ok) ok = mbar_wait(smem_addr(&M.stats_full[kpar]), (uint32_t)((k >> 1) & 1), abort);
             tc_fence_after();
             const bool split = p.n_splits > 1;
