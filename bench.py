@@ -9,7 +9,8 @@ A step is one pass of the whole path over one batch of synthetic input:
 The metric is query-heads per second (b * s * h per step time).  `value` is device time with
 inputs resident in HBM (L2 flushed between steps, each step timed with CUDA events on the
 launching stream); `e2e` times the same step through the public API with the step's inputs
-copied from pinned host memory and the output read back.  `roofline` relates the sparse_attn
+copied from pinned host memory and the output read back, the queries in parts (--e2e-chunks)
+whose copies in and out overlap the attention of other parts.  `roofline` relates the sparse_attn
 launch to the binding roofline (HBM bytes or dense bf16 FLOPs), and `cpu_baseline` times the CPU
 oracle on a bounded sample of the same workload.
 
@@ -49,9 +50,9 @@ L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 # from the ncu captures summarised under profiles/, keyed by (hash of the CUDA sources the capture
 # ran, workload).  Any change to the sources makes the key miss, so a stale figure reads as null.
 NCU_TRAFFIC = {
-    ("6f457e81f12d8228", "swa_prefill"): 500_314_624,
-    ("6f457e81f12d8228", "cmp_prefill"): 1_065_895_936,
-    ("6f457e81f12d8228", "decode"): 83_265_280,
+    ("8dd4dac08f8264d9", "swa_prefill"): 500_228_096,
+    ("8dd4dac08f8264d9", "cmp_prefill"): 1_066_547_968,
+    ("8dd4dac08f8264d9", "decode"): 83_033_344,
 }
 
 
@@ -274,6 +275,43 @@ class GpuPath:
 
     def step(self, ev=None):
         """One pass of the path; ev = (start, end) CUDA events bracketing sparse_attn."""
+        self.prologue()
+        if ev is not None:
+            ev[0].record()
+        self.attn()
+        if ev is not None:
+            ev[1].record()
+
+    def chunks(self, n):
+        """n contiguous parts of the step's queries: (slice of q / idx / o, slice of kv).  Batched
+        decode splits the sequences, a prefill (b = 1) its query tokens."""
+        wl = self.wl
+        if wl.b > 1:
+            edges = np.linspace(0, wl.b, min(n, wl.b) + 1).astype(int)
+            return [((slice(a, b),), (slice(a, b),)) for a, b in zip(edges, edges[1:]) if b > a]
+        edges = np.linspace(0, wl.s, min(n, wl.s) + 1).astype(int)
+        return [((slice(None), slice(a, b)), (slice(None),)) for a, b in zip(edges, edges[1:]) if b > a]
+
+    def attn(self, part=None, workspace=None):
+        """sparse_attn over every query, or over one part from chunks() (on the current stream)."""
+        wl = self.wl
+        qs, ks = part if part is not None else ((slice(None),), (slice(None),))
+        self.sa.sparse_attn(self.q[qs], self.kv[ks], self.sink, self.idx[qs], wl.scale,
+                            kv_scale=None if self.kv_scale is None else self.kv_scale[ks],
+                            out=self.o[qs], workspace=self.ws if workspace is None else workspace)
+
+    def workspace_for(self, parts):
+        """A workspace large enough for every part (fewer queries can mean more split scratch)."""
+        wl, sa = self.wl, self.sa
+        fmt = sa.SA_KV_FP8_E4M3 if self.fp8 else sa.SA_KV_BF16
+        need = max(sa.workspace_size(*self.q[qs].shape[:2], wl.h, wl.d, wl.rows, wl.topk, fmt)
+                   for qs, _ in parts)
+        if need <= self.ws.numel():
+            return self.ws
+        return self.torch.zeros(need, dtype=self.torch.uint8, device=self.dev)
+
+    def prologue(self):
+        """The step's window index table and the re-quantisation of the rows it owns."""
         sa, wl, d = self.sa, self.wl, self.wl.d
         sa.window_idxs(wl.start_pos, wl.s, wl.window, out=self.idx[:, :, : wl.window], nbatch=wl.b)
         if self.decode:
@@ -285,12 +323,6 @@ class GpuPath:
         else:
             nr = self.new_rows.view(-1, d)
             sa.act_quant_fp8(nr, out_rt=self.kv[:, : wl.s, :].reshape(-1, d))
-        if ev is not None:
-            ev[0].record()
-        sa.sparse_attn(self.q, self.kv, self.sink, self.idx, wl.scale, kv_scale=self.kv_scale,
-                       out=self.o, workspace=self.ws)
-        if ev is not None:
-            ev[1].record()
 
 
 def run_gpu(args, rank, world, local):
@@ -341,14 +373,39 @@ def run_gpu(args, rank, world, local):
            (pin["idx"].numel() * 4 if pin["idx"] is not None else 0))
     d2h = pin["o"].numel() * 2
 
+    # The queries go in, are attended and come back out in parts, on three streams, so that the
+    # copies of one part overlap the compute of another (every byte still crosses the link every
+    # step, and every output is computed); --e2e-chunks 1 is the plain serial step.
+    # (default: one part per 256 query tokens, at most 16 -- parts large enough to fill the GPU
+    # without splitting their index columns; a decode batch stays whole)
+    n_parts = args.e2e_chunks if args.e2e_chunks > 0 else max(1, min(16, wl.n_tokens // 256))
+    parts = path.chunks(n_parts)
+    ws_parts = path.workspace_for(parts)
+    s_in, s_cmp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+
     def e2e_step():
-        path.q.copy_(pin["q"], non_blocking=True)
+        cur = torch.cuda.current_stream()
+        # the previous step's compute has read q, kv and idx, and its copies out have read o
+        cur.wait_stream(s_cmp)
+        cur.wait_stream(s_out)
+        s_in.wait_stream(cur)
         path.new_rows.copy_(pin["rows"], non_blocking=True)
         path.sink.copy_(pin["sink"], non_blocking=True)
         if pin["idx"] is not None:
             path.idx.copy_(pin["idx"], non_blocking=True)
-        path.step()
-        pin["o"].copy_(path.o, non_blocking=True)
+        path.prologue()
+        s_cmp.wait_stream(cur)
+        for part in parts:
+            qs = part[0]
+            with torch.cuda.stream(s_in):
+                path.q[qs].copy_(pin["q"][qs], non_blocking=True)
+            s_cmp.wait_stream(s_in)
+            with torch.cuda.stream(s_cmp):
+                path.attn(part, ws_parts)
+            s_out.wait_stream(s_cmp)
+            with torch.cuda.stream(s_out):
+                pin["o"][qs].copy_(path.o[qs], non_blocking=True)
+        cur.wait_stream(s_out)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -411,7 +468,7 @@ def run_gpu(args, rank, world, local):
         "roofline": roof,
         "e2e": {"value": round(job_value(units, world, ms_e2e / 1e3), 1), "unit": UNIT,
                 "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h), "parts": len(parts)},
         "gpu_launches": path.launches_per_step * args.steps,
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "lib_version": lib_version,
@@ -572,6 +629,9 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="parts the end-to-end step's queries are copied and attended in "
+                         "(0: one per 256 query tokens, at most 16)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

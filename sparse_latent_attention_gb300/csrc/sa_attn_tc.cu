@@ -29,7 +29,8 @@
 //               cp.async 16 B into the swizzled layout (fp8 rows are staged raw and widened in
 //               place); rows already resident from the previous pair are kept -- see below
 //   warps 6-9   softmax: S -> P (bf16, shared memory), running max and sum, O rescale
-//   warps 10-13 epilogue: O^T -> o (bf16) or split partials
+//   warps 10-13 epilogue: O^T -> o (bf16) or split partials; with fp8 kv, between epilogues,
+//               they widen the second half (d 256-511) of every staged tile
 // Every wait is bounded; a wait that gives up raises the timeout bit and every role unwinds.
 //
 // Row placement.  The order of the gathered rows inside a tile does not matter (the softmax and
