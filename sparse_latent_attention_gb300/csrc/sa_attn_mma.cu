@@ -352,7 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(Params p) {
 // Merge the split partials of one token: M = max_s m_s;
 // o = sum_s 2^(m_s - M) O_s / (2^(sink log2e - M) + sum_s 2^(m_s - M) l_s), zero when no row.
 // One block of d / 4 threads per (token, head): thread i merges columns 4 i .. 4 i + 3 of the
-// split partials.  (The few split statistics every thread reads stay in L1.)
+// split partials in one pass over the splits, four at a time (their statistics and partial
+// columns are loaded together, so the loads of a group overlap), rescaling its running sums
+// whenever a split raises the maximum.  Splits with l = 0 (no row) are skipped.
 __global__ void attn_combine_kernel(const float* __restrict__ part_ml,
                                     const float* __restrict__ part_o,
                                     const float* __restrict__ sink, __nv_bfloat16* __restrict__ o,
@@ -361,31 +363,42 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_ml,
     const int hh = (int)(th % h);
     const int64_t token = th / h;
     const int c = 4 * threadIdx.x;
-    const float* ml0 = part_ml + (token * n_splits * (int64_t)h + hh) * 2;  // split 0
-    const int64_t ml_step = (int64_t)h * 2;                                  // next split
+    const float2* ml0 = reinterpret_cast<const float2*>(part_ml) + token * n_splits * (int64_t)h + hh;
+    const float* po0 = part_o + (token * n_splits * (int64_t)h + hh) * d + c;
     float M = -INFINITY, L = 0.f;
-    for (int sp = 0; sp < n_splits; ++sp) {
-        const float* ml = ml0 + sp * ml_step;
-        if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < n_splits; s0 += 4) {
+        float2 ml[4];
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool in = s0 + i < n_splits;
+            ml[i] = in ? ml0[(int64_t)(s0 + i) * h] : make_float2(0.f, 0.f);
+            v[i] = in ? *reinterpret_cast<const float4*>(po0 + (int64_t)(s0 + i) * h * d)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (!(ml[i].y > 0.f)) continue;
+            if (ml[i].x > M) {  // a new maximum: rescale what was summed so far (0 at the start)
+                const float r = M == -INFINITY ? 0.f : fast_exp2(M - ml[i].x);
+                L *= r;
+                acc.x *= r;
+                acc.y *= r;
+                acc.z *= r;
+                acc.w *= r;
+                M = ml[i].x;
+            }
+            const float w = fast_exp2(ml[i].x - M);
+            L += w * ml[i].y;
+            acc.x += w * v[i].x;
+            acc.y += w * v[i].y;
+            acc.z += w * v[i].z;
+            acc.w += w * v[i].w;
+        }
     }
     const float Mu = M == -INFINITY ? 0.f : M;
-    for (int sp = 0; sp < n_splits; ++sp) {
-        const float* ml = ml0 + sp * ml_step;
-        if (ml[1] > 0.f) L += ml[1] * fast_exp2(ml[0] - Mu);
-    }
     const float inv = L > 0.f ? 1.f / (L + fast_exp2(sink[hh] * kLog2e - Mu)) : 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sp = 0; sp < n_splits; ++sp) {
-        const float* ml = ml0 + sp * ml_step;
-        if (!(ml[1] > 0.f)) continue;
-        const float w = fast_exp2(ml[0] - Mu);
-        const float4 v = *reinterpret_cast<const float4*>(
-            part_o + ((token * n_splits + sp) * h + hh) * (int64_t)d + c);
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
-    }
     uint2 out;
     out.x = pack_bf16(acc.x * inv, acc.y * inv);
     out.y = pack_bf16(acc.z * inv, acc.w * inv);
