@@ -519,9 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     j = -1;
                 }
                 // ring placement (slot = j mod 128) when the valid rows' residues are distinct
-                // (the per-pair records rotate over three entries: the one for the pair after
-                // this is cleared after this pair's barrier, and is next written after the
-                // next pair's barrier)
+                // (the per-pair records rotate over three entries; the previous pair's is cleared
+                // after this pair's barrier, when nobody reads it any more, and is next written
+                // by the pair after the next, after the next pair's barrier.  The next pair's
+                // own entry must not be touched here: a fast thread may be filling it already.)
                 if (j >= 0) {
                     atomicOr(&M.ring_bits[g3][(j & 127) >> 5], 1u << (j & 31));
                     atomicAdd(&M.ring_count[g3], 1);
@@ -545,9 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool copy = j >= 0 && !(same_seq && M.row_id[ps] == j);
                 if (j >= 0) M.row_id[ps] = j;
                 if (pt == 0) {
-                    M.ring_bits[gnext][0] = M.ring_bits[gnext][1] = 0;
-                    M.ring_bits[gnext][2] = M.ring_bits[gnext][3] = 0;
-                    M.ring_count[gnext] = 0;
+                    M.ring_bits[gprev][0] = M.ring_bits[gprev][1] = 0;
+                    M.ring_bits[gprev][2] = M.ring_bits[gprev][3] = 0;
+                    M.ring_count[gprev] = 0;
                 }
                 g3 = gnext;
                 // the claimed slots (16 of each tile: slots 16 pw .. 16 pw + 15 in the first
