@@ -50,9 +50,9 @@ L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 # from the ncu captures summarised under profiles/, keyed by (hash of the CUDA sources the capture
 # ran, workload).  Any change to the sources makes the key miss, so a stale figure reads as null.
 NCU_TRAFFIC = {
-    ("8dd4dac08f8264d9", "swa_prefill"): 500_228_096,
-    ("8dd4dac08f8264d9", "cmp_prefill"): 1_066_547_968,
-    ("8dd4dac08f8264d9", "decode"): 83_033_344,
+    ("809a7d6c2a3e885c", "swa_prefill"): 500_622_848,
+    ("809a7d6c2a3e885c", "cmp_prefill"): 1_066_425_088,
+    ("809a7d6c2a3e885c", "decode"): 82_903_552,
 }
 
 
