@@ -246,6 +246,25 @@ def test_running_max_raised_every_tile(dev):
     assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what="growing logits")
 
 
+def test_query_parts_match_the_whole_call(dev):
+    # Attending the query tokens in parts (as the benchmark's end-to-end step does, each part its
+    # own call on the same kv) gives the whole call's output bit for bit: a token's result does
+    # not depend on which other tokens share the call.
+    wl = workloads.make_random(1, 1200, 64, 512, 1400, 200, seed=4242, window=128)
+    x = _gpu.prepare(wl, dev, quantise=False)
+    ws = sa.new_workspace(1, 1200, 64, 512, 1400, 200, device=dev)
+    whole = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, workspace=ws)
+    parts = torch.empty_like(whole)
+    for a, b in ((0, 256), (256, 512), (512, 1000), (1000, 1200)):
+        wp = sa.new_workspace(1, b - a, 64, 512, 1400, 200, device=dev)
+        sa.sparse_attn(x["q"][:, a:b], x["kv"], x["sink"], x["idx"][:, a:b], wl.scale,
+                       out=parts[:, a:b], workspace=wp)
+        assert sa.read_status(wp) == 0
+    torch.cuda.synchronize()
+    assert sa.read_status(ws) == 0
+    assert torch.equal(whole.view(torch.int16), parts.view(torch.int16))
+
+
 def test_sink_minus_inf_and_single_row(dev):
     wl = workloads.make_random(2, 5, 64, 512, 40, 24, seed=77, neg_frac=0.0)
     wl.sink[:] = -np.inf
