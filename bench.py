@@ -331,7 +331,7 @@ def run_gpu(args, rank, world, local):
     dev = torch.device("cuda", local)
     rank0 = rank == 0
     peaks = load_peaks()
-    wl = workloads.make_named(args.workload)
+    wl = workloads.make_named(args.workload, batch=args.batch)
     path = GpuPath(wl, dev)
     path.step()
     torch.cuda.synchronize()
@@ -591,7 +591,7 @@ def cpu_baseline(wl, budget_s=12.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    wl = workloads.make_named(args.workload)
+    wl = workloads.make_named(args.workload, batch=args.batch)
     step = OracleStep(wl)
     probe = step.next_tokens(min(8, wl.n_tokens))
     step.prepare(probe)
@@ -640,6 +640,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="sequences of a decode workload (a smaller case for profiler captures)")
     ap.add_argument("--e2e-chunks", type=int, default=0,
                     help="parts the end-to-end step's queries are copied and attended in "
                          "(0: one per 256 query tokens, at most 16)")

@@ -104,8 +104,10 @@ def _fill_rows(rng, b, rows_per_seq, d):
 
 
 @functools.lru_cache(maxsize=4)
-def make_named(name: str, visibility: str = "pages") -> Workload:
-    """One of the five named workloads, drawn from its fixed seed."""
+def make_named(name: str, visibility: str = "pages", batch: int | None = None) -> Workload:
+    """One of the five named workloads, drawn from its fixed seed.  ``batch`` sets the number of
+    sequences of the two decode workloads (a smaller case of the same structure, e.g. for a
+    profiler capture); the other workloads ignore it."""
     if name == "tiny":
         seed, b, s, h, d, rows, W = 1, 1, 16, 4, 64, 48, 8
         rng = np.random.default_rng(seed)
@@ -150,6 +152,8 @@ def make_named(name: str, visibility: str = "pages") -> Workload:
             seed, b, h, pos, k, n_drop, fmt = 4, 64, 64, 32768, 1024, 0, "bf16"
         else:
             seed, b, h, pos, k, n_drop, fmt = 5, 256, 128, 131072, 2048, 102, "fp8"
+        if batch is not None:
+            b = int(batch)
         s, d, W, ratio = 1, 512, 128, 4
         n_cmp = pos // ratio
         rng = np.random.default_rng(seed)
