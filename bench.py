@@ -314,12 +314,13 @@ class GpuPath:
         """The step's window index table and the re-quantisation of the rows it owns."""
         sa, wl, d = self.sa, self.wl, self.wl.d
         sa.window_idxs(wl.start_pos, wl.s, wl.window, out=self.idx[:, :, : wl.window], nbatch=wl.b)
-        if self.decode:
+        if self.decode:  # the step's token enters each sequence's ring (its first window rows)
+            x = self.new_rows[:, None, :]
             if self.fp8:
-                sa.act_quant_fp8(self.new_rows, codes=self.kv[:, self.slot, :],
-                                 scales=self.kv_scale[:, self.slot, :])
+                sa.window_write(x, wl.start_pos, codes=self.kv[:, : wl.window],
+                                scales=self.kv_scale[:, : wl.window])
             else:
-                sa.act_quant_fp8(self.new_rows, out_rt=self.kv[:, self.slot, :])
+                sa.window_write(x, wl.start_pos, ring_rt=self.kv[:, : wl.window])
         else:
             nr = self.new_rows.view(-1, d)
             sa.act_quant_fp8(nr, out_rt=self.kv[:, : wl.s, :].reshape(-1, d))

@@ -159,6 +159,36 @@ sa_status sa_act_quant_fp8(const void* x, int64_t n, int d, int64_t x_stride,
                            uint8_t* scales, int64_t scales_stride, void* stream);
 
 /*
+ * Ring write: the window cache's write side, with act_quant fused.
+ *
+ * Source: "Module attn" API page, the ring-cache paragraph (the kv row of the token at position t
+ * is kept in slot t mod window; a later token overwrites an earlier one in the same slot) and
+ * act_quant_inplace (the kv row is quantised before it is stored).
+ *
+ * For each of `nbatch` sequences, the kv rows of `seqlen` new tokens at positions
+ * start_pos .. start_pos + seqlen - 1 go to ring slot (position mod window) of that sequence,
+ * quantised exactly as sa_act_quant_fp8 quantises a row.  When seqlen > window only the last
+ * `window` tokens are written (each earlier token's slot is taken by a later one), so the ring ends
+ * as if every token had been written in order.
+ *   x            the new rows, bf16: row t of sequence bi at x + (bi * seqlen + t) * x_stride
+ *                elements (x_stride >= d)
+ *   ring_rt      bf16 round trip c * s: row `slot` of sequence bi at
+ *                ring_rt + bi * rt_batch_stride + slot * rt_stride elements, or NULL
+ *   ring_codes   e4m3 bytes, addressed the same way with codes_stride / codes_batch_stride, or NULL
+ *   ring_scales  e8m0 bytes (d / 32 per row), scales_stride / scales_batch_stride, or NULL
+ * At least one output; the ring rows of one sequence must not overlap those of another, and no
+ * output may overlap x.  Requires d % 32 == 0, d >= 32, window >= 1, and non-negative nbatch,
+ * seqlen and start_pos.  Returns SA_ERR_INVALID_ARG (nothing enqueued) for a bad argument and
+ * SA_ERR_CUDA for a launch error; the caller owns every buffer.
+ */
+sa_status sa_window_write(const void* x, int64_t nbatch, int64_t seqlen, int d, int64_t x_stride,
+                          int64_t start_pos, int window,
+                          void* ring_rt, int64_t rt_stride, int64_t rt_batch_stride,
+                          uint8_t* ring_codes, int64_t codes_stride, int64_t codes_batch_stride,
+                          uint8_t* ring_scales, int64_t scales_stride, int64_t scales_batch_stride,
+                          void* stream);
+
+/*
  * Reads the status word in a workspace (synchronises `stream` first) and returns SA_OK or the
  * error recorded there: SA_ERR_TIMEOUT (a kernel wait gave up) before SA_ERR_INDEX (an index
  * outside [-1, rows) was seen).  With clear != 0 the word is reset to zero.

@@ -147,6 +147,47 @@ def act_quant_fp8(x, *, out_rt=None, codes=None, scales=None, stream=None):
     _lib.check(st, "sa_act_quant_fp8")
 
 
+def window_write(x, start_pos, *, ring_rt=None, codes=None, scales=None, stream=None):
+    """The ring write with act_quant fused (sa_window_write): row t of x[bi] (the new token at
+    position start_pos + t of sequence bi) goes to ring slot (start_pos + t) % window.
+
+    x is a 3-D CUDA bf16 tensor [nbatch, seqlen, d] (last dim contiguous, rows of a sequence
+    equally spaced, sequences seqlen rows apart).  The rings are 3-D tensors [nbatch, window, d]
+    (bf16 round trip ``ring_rt``, e4m3 ``codes``) or [nbatch, window, d / 32] (e8m0 ``scales``)
+    with unit column stride; they may be strided views of a larger cache, e.g. its first window
+    rows."""
+    if x.dim() != 3 or x.stride(2) != 1 or x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise ValueError("x must be a 3-D CUDA bf16 tensor with unit column stride")
+    nb, sl, d = x.shape
+    if nb > 1 and x.stride(0) != sl * x.stride(1):
+        raise ValueError("the sequences of x must be seqlen rows apart")
+    window = None
+
+    def ring_of(t, name, dtype, width):
+        nonlocal window
+        if t is None:
+            return None, 0, 0
+        if (t.dim() != 3 or t.dtype != dtype or t.stride(2) != 1 or t.shape[0] != nb
+                or t.shape[2] != width):
+            raise ValueError(f"{name} must be a 3-D {dtype} tensor of shape ({nb}, window, {width})"
+                             " with unit column stride")
+        if window is None:
+            window = t.shape[1]
+        elif t.shape[1] != window:
+            raise ValueError("the rings must have the same window")
+        return t, t.stride(1), t.stride(0)
+
+    rt, rts, rtb = ring_of(ring_rt, "ring_rt", torch.bfloat16, d)
+    cd, cds, cdb = ring_of(codes, "codes", torch.uint8, d)
+    sc, scs, scb = ring_of(scales, "scales", torch.uint8, d // 32)
+    if window is None:
+        raise ValueError("give at least one of ring_rt, codes, scales")
+    st = load().sa_window_write(_ptr(x), nb, sl, d, x.stride(1) if sl > 1 else d, int(start_pos),
+                                window, _ptr(rt), rts, rtb, _ptr(cd), cds, cdb, _ptr(sc), scs, scb,
+                                _stream(stream))
+    _lib.check(st, "sa_window_write")
+
+
 def read_status(workspace, clear=False, stream=None) -> int:
     """The workspace status word as an sa_status (synchronises the stream)."""
     return int(load().sa_read_status(_ptr(workspace), int(bool(clear)), _stream(stream)))

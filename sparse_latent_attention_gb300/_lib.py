@@ -53,6 +53,9 @@ def load() -> ctypes.CDLL:
         lib.sa_window_idxs.argtypes = [i64, i64, i32, P, i64, i64, i64, P]
         lib.sa_act_quant_fp8.restype = i32
         lib.sa_act_quant_fp8.argtypes = [P, i64, i32, i64, P, i64, P, i64, P, i64, P]
+        lib.sa_window_write.restype = i32
+        lib.sa_window_write.argtypes = [P, i64, i64, i32, i64, i64, i32, P, i64, i64, P, i64, i64,
+                                        P, i64, i64, P]
         lib.sa_read_status.restype = i32
         lib.sa_read_status.argtypes = [P, i32, P]
         lib.sa_status_string.restype = ctypes.c_char_p

@@ -137,6 +137,43 @@ sa_status sa_act_quant_fp8(const void* x, int64_t n, int d, int64_t x_stride, vo
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+sa_status sa_window_write(const void* x, int64_t nbatch, int64_t seqlen, int d, int64_t x_stride,
+                          int64_t start_pos, int window, void* ring_rt, int64_t rt_stride,
+                          int64_t rt_batch_stride, uint8_t* ring_codes, int64_t codes_stride,
+                          int64_t codes_batch_stride, uint8_t* ring_scales, int64_t scales_stride,
+                          int64_t scales_batch_stride, void* stream) {
+    if (nbatch < 0 || seqlen < 0 || start_pos < 0 || window < 1 || d < 32 || d % 32 != 0)
+        return SA_ERR_INVALID_ARG;
+    if (!ring_rt && !ring_codes && !ring_scales) return SA_ERR_INVALID_ARG;
+    if (nbatch == 0 || seqlen == 0) return SA_OK;
+    if (!x || !aligned(x, 2) || x_stride < d) return SA_ERR_INVALID_ARG;
+    // each sequence's ring: its rows, and the batch stride that keeps the rings apart
+    const int64_t w1 = window - 1;
+    if (ring_rt && (!aligned(ring_rt, 2) || rt_stride < d ||
+                    (nbatch > 1 && rt_batch_stride < w1 * rt_stride + d)))
+        return SA_ERR_INVALID_ARG;
+    if (ring_codes && (codes_stride < d || (nbatch > 1 && codes_batch_stride < w1 * codes_stride + d)))
+        return SA_ERR_INVALID_ARG;
+    if (ring_scales && (scales_stride < d / 32 ||
+                        (nbatch > 1 && scales_batch_stride < w1 * scales_stride + d / 32)))
+        return SA_ERR_INVALID_ARG;
+    const size_t x_bytes = (size_t)((nbatch * seqlen - 1) * x_stride + d) * 2;
+    if (ring_rt && overlaps(ring_rt, (size_t)((nbatch - 1) * rt_batch_stride + w1 * rt_stride + d) * 2,
+                            x, x_bytes))
+        return SA_ERR_INVALID_ARG;
+    if (ring_codes && overlaps(ring_codes, (size_t)((nbatch - 1) * codes_batch_stride + w1 * codes_stride + d),
+                               x, x_bytes))
+        return SA_ERR_INVALID_ARG;
+    if (ring_scales && overlaps(ring_scales,
+                                (size_t)((nbatch - 1) * scales_batch_stride + w1 * scales_stride + d / 32),
+                                x, x_bytes))
+        return SA_ERR_INVALID_ARG;
+    return from_cuda(sa::window_write_launch(x, nbatch, seqlen, d, x_stride, start_pos, window, ring_rt,
+                                             rt_stride, rt_batch_stride, ring_codes, codes_stride,
+                                             codes_batch_stride, ring_scales, scales_stride,
+                                             scales_batch_stride, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 sa_status sa_read_status(void* workspace, int clear, void* stream) {
     if (!workspace || !aligned(workspace, 4)) return SA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

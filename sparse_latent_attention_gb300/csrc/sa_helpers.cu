@@ -72,6 +72,22 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
 
 // One warp per 32-element block: lane k owns element k.  x_rt may alias x (in place): a lane
 // reads its element before the block maximum is formed and writes it only afterwards.
+// One 32-element block of a row, one element per lane of a converged warp: amax (floored at
+// 1e-4), s = pow2_ceil(amax / 448), the e4m3 code of v / s and the bf16 round trip code * s;
+// writes whichever of rt / code / scale (lane 0) are given.
+__device__ __forceinline__ void quant_block32(float v, int lane, __nv_bfloat16* rt, uint8_t* code,
+                                              uint8_t* scale) {
+    // |v| orders like its bit pattern, so the block maximum is an integer max
+    const uint32_t abits = __float_as_uint(v) & 0x7FFFFFFFu;
+    float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, abits));
+    if (amax < 1e-4f) amax = 1e-4f;
+    const float sc = pow2_ceil_bits(__fdiv_rn(amax, 448.0f));
+    const uint8_t c = f32_to_e4m3_sat(__fdiv_rn(v, sc));
+    if (code) *code = c;
+    if (rt) *rt = __float2bfloat16_rn(e4m3_to_f32(c) * sc);
+    if (scale && lane == 0) *scale = (uint8_t)((__float_as_uint(sc) >> 23) & 0xFFu);
+}
+
 __global__ void act_quant_kernel(const __nv_bfloat16* x, int64_t n, int d,
                                  int64_t xs, __nv_bfloat16* x_rt, int64_t rts,
                                  uint8_t* __restrict__ codes, int64_t cs,
@@ -85,16 +101,39 @@ __global__ void act_quant_kernel(const __nv_bfloat16* x, int64_t n, int d,
         const int64_t r = blk / blocks_per_row;
         const int cb = (int)(blk - r * blocks_per_row);
         const int64_t col = (int64_t)cb * 32 + lane;
-        const float v = __bfloat162float(x[r * xs + col]);
-        // |v| orders like its bit pattern, so the block maximum is an integer max
-        const uint32_t abits = __float_as_uint(v) & 0x7FFFFFFFu;
-        float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, abits));
-        if (amax < 1e-4f) amax = 1e-4f;
-        const float sc = pow2_ceil_bits(__fdiv_rn(amax, 448.0f));
-        const uint8_t c = f32_to_e4m3_sat(__fdiv_rn(v, sc));
-        if (codes) codes[r * cs + col] = c;
-        if (x_rt) x_rt[r * rts + col] = __float2bfloat16_rn(e4m3_to_f32(c) * sc);
-        if (scales && lane == 0) scales[r * ss + cb] = (uint8_t)((__float_as_uint(sc) >> 23) & 0xFFu);
+        quant_block32(__bfloat162float(x[r * xs + col]), lane, x_rt ? x_rt + r * rts + col : nullptr,
+                      codes ? codes + r * cs + col : nullptr, scales ? scales + r * ss + cb : nullptr);
+    }
+}
+
+// Ring write ([attn-doc] ring-cache paragraph): new token t (of seqlen, at position
+// start_pos + t) of sequence bi goes to ring slot (start_pos + t) mod window, quantised as
+// act_quant_kernel quantises.  Only the last min(seqlen, window) tokens are written: an earlier
+// token's slot belongs to a later one.  Source row (bi, t) at x + (bi * seqlen + t) * xs; ring row
+// (bi, slot) at base + bi * batch stride + slot * row stride.
+__global__ void window_write_kernel(const __nv_bfloat16* x, int64_t nbatch, int64_t seqlen, int d,
+                                    int64_t xs, int64_t start_pos, int window,
+                                    __nv_bfloat16* rt, int64_t rts, int64_t rtb,
+                                    uint8_t* __restrict__ codes, int64_t cs, int64_t cbs,
+                                    uint8_t* __restrict__ scales, int64_t ss, int64_t sbs) {
+    const int lane = threadIdx.x & 31;
+    const int blocks_per_row = d / 32;
+    const int64_t t_first = seqlen > window ? seqlen - window : 0;
+    const int64_t per_seq = seqlen - t_first;
+    const int64_t total = nbatch * per_seq * blocks_per_row;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t blk = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; blk < total;
+         blk += warps) {
+        const int64_t row = blk / blocks_per_row;
+        const int cb = (int)(blk - row * blocks_per_row);
+        const int64_t bi = row / per_seq;
+        const int64_t t = t_first + (row - bi * per_seq);
+        const int64_t slot = (start_pos + t) % window;
+        const int64_t col = (int64_t)cb * 32 + lane;
+        quant_block32(__bfloat162float(x[(bi * seqlen + t) * xs + col]), lane,
+                      rt ? rt + bi * rtb + slot * rts + col : nullptr,
+                      codes ? codes + bi * cbs + slot * cs + col : nullptr,
+                      scales ? scales + bi * sbs + slot * ss + cb : nullptr);
     }
 }
 
@@ -125,6 +164,21 @@ cudaError_t act_quant_launch(const void* x, int64_t n, int d, int64_t x_stride, 
     act_quant_kernel<<<grid_for(total_threads, 256), 256, 0, stream>>>(
         (const __nv_bfloat16*)x, n, d, x_stride, (__nv_bfloat16*)x_rt, rt_stride, codes,
         codes_stride, scales, scales_stride);
+    return cudaGetLastError();
+}
+
+cudaError_t window_write_launch(const void* x, int64_t nbatch, int64_t seqlen, int d,
+                                int64_t x_stride, int64_t start_pos, int window, void* ring_rt,
+                                int64_t rt_stride, int64_t rt_batch_stride, uint8_t* codes,
+                                int64_t codes_stride, int64_t codes_batch_stride, uint8_t* scales,
+                                int64_t scales_stride, int64_t scales_batch_stride,
+                                cudaStream_t stream) {
+    const int64_t rows = nbatch * (seqlen < window ? seqlen : (int64_t)window);
+    if (rows * d == 0) return cudaSuccess;
+    window_write_kernel<<<grid_for(rows * d, 256), 256, 0, stream>>>(
+        (const __nv_bfloat16*)x, nbatch, seqlen, d, x_stride, start_pos, window,
+        (__nv_bfloat16*)ring_rt, rt_stride, rt_batch_stride, codes, codes_stride, codes_batch_stride,
+        scales, scales_stride, scales_batch_stride);
     return cudaGetLastError();
 }
 

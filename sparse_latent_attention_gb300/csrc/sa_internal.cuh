@@ -52,6 +52,12 @@ cudaError_t attn_tc_launch(const AttnCall& c);
 cudaError_t window_idxs_launch(int64_t start_pos, int64_t seqlen, int window, int32_t* idx,
                                int64_t ld, int64_t nbatch, int64_t batch_stride,
                                cudaStream_t stream);
+cudaError_t window_write_launch(const void* x, int64_t nbatch, int64_t seqlen, int d,
+                                int64_t x_stride, int64_t start_pos, int window, void* ring_rt,
+                                int64_t rt_stride, int64_t rt_batch_stride, uint8_t* codes,
+                                int64_t codes_stride, int64_t codes_batch_stride, uint8_t* scales,
+                                int64_t scales_stride, int64_t scales_batch_stride,
+                                cudaStream_t stream);
 cudaError_t act_quant_launch(const void* x, int64_t n, int d, int64_t x_stride, void* x_rt,
                              int64_t rt_stride, uint8_t* codes, int64_t codes_stride,
                              uint8_t* scales, int64_t scales_stride, cudaStream_t stream);

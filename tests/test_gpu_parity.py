@@ -147,6 +147,43 @@ def test_act_quant_every_bf16_value(dev):
         assert (sc.cpu().numpy() == want_sc).all(), amax
 
 
+@pytest.mark.parametrize("nb,seqlen,start_pos,window,rows", [
+    (1, 12, 0, 8, 8),          # the ring-cache paragraph's prefill: 12 tokens into 8 slots
+    (2, 12, 0, 8, 20),         # the same for two sequences, the ring the first 8 rows of a cache
+    (2, 5, 0, 8, 8),           # fewer tokens than slots
+    (3, 1, 13, 8, 30),         # decode at position 13 (slot 5)
+    (3, 1, 32768, 128, 300),   # decode at position 32768 (slot 0) into a 128-slot ring
+    (1, 300, 0, 128, 128)])    # a long prefill: only the last 128 tokens stay
+def test_window_write_bit_exact(dev, nb, seqlen, start_pos, window, rows):
+    d = 512
+    rng = np.random.default_rng(900 + nb * 31 + seqlen)
+    x = rng.standard_normal((nb, seqlen, d)).astype(np.float32)
+    x *= np.exp(rng.uniform(-20, 20, (nb, seqlen, d // 32))).repeat(32, axis=2).astype(np.float32)
+    bits = workloads.to_bf16_bits(x)
+    rt, codes, sc = oracle.act_quant(bits.reshape(-1, d))
+    rt, codes, sc = (a.reshape(nb, seqlen, -1) for a in (rt, codes, sc))
+    # expected caches: a sentinel everywhere, the ring rows placed by the oracle's ring write
+    want_rt = np.full((nb, rows, d), 0x3F80, np.uint16)
+    want_c = np.full((nb, rows, d), 0xAB, np.uint8)
+    want_s = np.full((nb, rows, d // 32), 0x55, np.uint8)
+    for bi in range(nb):
+        ring = np.ascontiguousarray(want_rt[bi, :window])
+        oracle.ring_write(ring, rt[bi], start_pos)
+        want_rt[bi, :window] = ring
+        for t in range(seqlen):  # the codes and scales follow the same slot rule
+            want_c[bi, (start_pos + t) % window] = codes[bi, t]
+            want_s[bi, (start_pos + t) % window] = sc[bi, t]
+    cache_rt = torch.full((nb, rows, d), 1.0, dtype=torch.bfloat16, device=dev)
+    cache_c = torch.full((nb, rows, d), 0xAB, dtype=torch.uint8, device=dev)
+    cache_s = torch.full((nb, rows, d // 32), 0x55, dtype=torch.uint8, device=dev)
+    sa.window_write(_gpu.u16_to_bf16_tensor(bits, dev), start_pos, ring_rt=cache_rt[:, :window],
+                    codes=cache_c[:, :window], scales=cache_s[:, :window])
+    torch.cuda.synchronize()
+    assert (_gpu.bf16_tensor_to_u16(cache_rt) == want_rt).all()
+    assert (cache_c.cpu().numpy() == want_c).all()
+    assert (cache_s.cpu().numpy() == want_s).all()
+
+
 # --------------------------------------------------------------------------------------------
 # sparse_attn on the five named workloads (full size, sampled outputs)
 # --------------------------------------------------------------------------------------------

@@ -20,7 +20,7 @@ def test_exports_every_declared_symbol(lib):
     names = _lib.declared_symbols()
     assert set(names) == {"sa_sparse_attn", "sa_sparse_attn_workspace_size", "sa_window_idxs",
                           "sa_act_quant_fp8", "sa_read_status", "sa_status_string", "sa_version",
-                          "sa_sparse_attn_static_scratch"}
+                          "sa_sparse_attn_static_scratch", "sa_window_write"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -43,6 +43,7 @@ def test_workspace_size_is_host_arithmetic(lib):
 
 
 FAKE = ctypes.c_void_p(1 << 40)  # never dereferenced: every call below fails validation first
+FAKE2 = ctypes.c_void_p(1 << 41)  # a second such address, far from the first
 
 
 def _attn(lib, **kw):
@@ -89,6 +90,29 @@ def test_act_quant_rejects_bad_arguments(lib):
     assert f(FAKE, 4, 64, 64, None, 0, None, 0, None, 0, None) == _lib.SA_ERR_INVALID_ARG
     assert f(FAKE, 4, 64, 32, FAKE, 64, None, 0, None, 0, None) == _lib.SA_ERR_INVALID_ARG
     assert f(None, 0, 64, 64, FAKE, 64, None, 0, None, 0, None) == _lib.SA_OK
+
+
+def test_window_write_rejects_bad_arguments(lib):
+    f = lib.sa_window_write
+    ok_args = [FAKE, 2, 1, 64, 64, 5, 8, FAKE2, 64, 8 * 64, None, 0, 0, None, 0, 0, None]
+
+    def call(**kw):
+        a = list(ok_args)
+        for k, v in kw.items():
+            a[int(k[1:])] = v
+        return f(*a)
+
+    assert call(a3=33) == _lib.SA_ERR_INVALID_ARG                   # d not a multiple of 32
+    assert call(a6=0) == _lib.SA_ERR_INVALID_ARG                    # window < 1
+    assert call(a5=-1) == _lib.SA_ERR_INVALID_ARG                   # negative position
+    assert call(a7=None) == _lib.SA_ERR_INVALID_ARG                 # no output at all
+    assert call(a4=32) == _lib.SA_ERR_INVALID_ARG                   # x rows shorter than d
+    assert call(a8=32) == _lib.SA_ERR_INVALID_ARG                   # ring rows shorter than d
+    assert call(a9=7 * 64) == _lib.SA_ERR_INVALID_ARG               # two sequences' rings overlap
+    assert call(a7=FAKE) == _lib.SA_ERR_INVALID_ARG                 # the ring overlaps x
+    assert call(a7=None, a10=FAKE2, a11=64, a12=8 * 64 - 1) == _lib.SA_ERR_INVALID_ARG
+    assert call(a7=None, a13=FAKE2, a14=1, a15=16) == _lib.SA_ERR_INVALID_ARG  # scale rows < d/32
+    assert call(a1=0) == _lib.SA_OK and call(a2=0) == _lib.SA_OK   # nothing to write
 
 
 def test_read_status_rejects_null(lib):
