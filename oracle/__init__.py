@@ -62,6 +62,8 @@ def _load():
             lib.or_act_quant.argtypes = [P, i64, i64, P, P, P]
             lib.or_window_idxs.restype = ctypes.c_int
             lib.or_window_idxs.argtypes = [i64, i64, i64, P, i64]
+            lib.or_rope.restype = ctypes.c_int
+            lib.or_rope.argtypes = [P, i64, i64, i64, P, i64, P, ctypes.c_int, P]
             lib.or_ring_write.restype = ctypes.c_int
             lib.or_ring_write.argtypes = [P, P, i64, i64, i64, i64]
             for name in ("or_bf16_round_array", "or_e4m3_encode_array", "or_e4m3_decode_array",
@@ -164,6 +166,26 @@ def ring_write(ring: np.ndarray, rows: np.ndarray, start_pos: int) -> None:
     rc = lib.or_ring_write(_ptr(ring), _ptr(r), start_pos, r.shape[0], ring.shape[0], ring.shape[1])
     if rc != OK:
         raise ValueError(f"or_ring_write failed ({rc})")
+
+
+def rope(x, rot, pos, rope_dim, inverse, want_f64=False):
+    """apply_rotary_emb on the last ``rope_dim`` elements of each row of x (bf16 bits, [..., d]):
+    rows of x flattened in order, row r at position pos[r] of the table rot ([npos, rope_dim/2, 2]
+    f32 cos, sin); ``inverse`` conjugates the rotation.  Returns a new array (and, with want_f64,
+    the unrounded rotated values [rows, rope_dim])."""
+    lib = _load()
+    x = np.array(x, dtype=np.uint16, copy=True, order="C")
+    d = x.shape[-1]
+    n = x.size // d
+    r = _c(rot, np.float32)
+    p = _c(np.asarray(pos, dtype=np.int64).reshape(-1), np.int64)
+    assert p.size == n
+    x64 = np.empty((n, rope_dim), np.float64) if want_f64 else None
+    rc = lib.or_rope(_ptr(x), n, d, rope_dim, _ptr(r), r.shape[0], _ptr(p), int(bool(inverse)),
+                     _ptr(x64) if want_f64 else None)
+    if rc != OK:
+        raise ValueError(f"or_rope failed ({rc})")
+    return (x, x64) if want_f64 else x
 
 
 def sparse_attn(q, kv, sink, idx, scale, *, kv_scales=None, tokens=None, nthreads=None,

@@ -10,7 +10,8 @@
  *          the ring-cache paragraph, Constants: FP8_BLOCK, Functions: act_quant_inplace,
  *          pow2_ceil, sparse_attn, window_topk_idxs.
  *   [FWD]  "DeepSeek V4.1" attention page (attention/output, prefill): Attention.forward and
- *          Attention.__init__ (softmax_scale = head_dim ** -0.5, attn_sink per local head).
+ *          Attention.__init__ (softmax_scale = head_dim ** -0.5, attn_sink per local head),
+ *          apply_rotary_emb (the inverse rotation of the output's rope dims).
  *
  * Floating point: dot products, the softmax and the weighted sum are carried in f64; the only
  * rounding to a narrow type is the final bf16 round-to-nearest-even of o.  The act_quant steps
@@ -219,6 +220,39 @@ int or_ring_write(uint16_t* ring, const uint16_t* rows, int64_t start_pos, int64
     if (window <= 0 || seqlen < 0 || start_pos < 0 || d <= 0) return 1;
     for (int64_t t = 0; t < seqlen; ++t)
         memcpy(ring + ((start_pos + t) % window) * d, rows + t * d, (size_t)d * sizeof(uint16_t));
+    return 0;
+}
+
+/* [FWD] apply_rotary_emb (and its use on the attention output, Attention.forward): the last
+ * rope_dim elements of a row are read as rope_dim / 2 complex numbers x_{2k} + i x_{2k+1}; each is
+ * multiplied by the rotation of the row's position, c_k + i s_k, or by its conjugate c_k - i s_k
+ * (inverse), and written back as bf16.  The product is formed in f64 from the bf16 input and the
+ * f32 table (the page forms it in f32), then rounded to bf16 (nearest even); the other elements
+ * of the row are left as they are.
+ *   x    [nrows][d] bf16, in place;  rot [npos][rope_dim / 2][2] f32 (c_k, s_k);  pos [nrows]
+ *   x64  optional [nrows][rope_dim] f64: the unrounded rotated values
+ * Returns 1 on a bad argument (odd or oversized rope_dim, a position outside the table). */
+int or_rope(uint16_t* x, int64_t nrows, int64_t d, int64_t rope_dim, const float* rot,
+            int64_t npos, const int64_t* pos, int inverse, double* x64) {
+    if (rope_dim <= 0 || rope_dim % 2 || rope_dim > d || nrows < 0) return 1;
+    const int64_t half = rope_dim / 2, base = d - rope_dim;
+    for (int64_t r = 0; r < nrows; ++r) {
+        if (pos[r] < 0 || pos[r] >= npos) return 1;
+        for (int64_t k = 0; k < half; ++k) {
+            const double a = or_bf16_to_f64(x[r * d + base + 2 * k]);
+            const double b = or_bf16_to_f64(x[r * d + base + 2 * k + 1]);
+            const double c = (double)rot[(pos[r] * half + k) * 2 + 0];
+            const double sn = (inverse ? -1.0 : 1.0) * (double)rot[(pos[r] * half + k) * 2 + 1];
+            /* (a + i b)(c + i sn) = (a c - b sn) + i (a sn + b c) */
+            const double re = a * c - b * sn, im = a * sn + b * c;
+            if (x64) {
+                x64[r * rope_dim + 2 * k] = re;
+                x64[r * rope_dim + 2 * k + 1] = im;
+            }
+            x[r * d + base + 2 * k] = or_bf16_round(re);
+            x[r * d + base + 2 * k + 1] = or_bf16_round(im);
+        }
+    }
     return 0;
 }
 

@@ -397,3 +397,68 @@ def test_window_idxs_cases():
         oracle.window_idxs(4, 3, 8)
     # empty chunk
     assert oracle.window_idxs(0, 0, 8).shape == (0, 8)
+
+
+# --------------------------------------------------------------------------------------------
+# apply_rotary_emb ("DeepSeek V4.1" attention page: the rotation of the output's rope dims)
+# --------------------------------------------------------------------------------------------
+
+def _rope_case(seed, n=40, d=512, rd=64, npos=50):
+    rng = np.random.default_rng(seed)
+    x = oracle.bf16_round(rng.standard_normal((n, d)) * np.exp(rng.uniform(-5, 5, (n, d))))
+    ang = rng.uniform(-np.pi, np.pi, (npos, rd // 2))
+    rot = np.stack([np.cos(ang), np.sin(ang)], -1).astype(np.float32)
+    pos = rng.integers(0, npos, n)
+    return x, rot, pos, d, rd
+
+
+@pytest.mark.parametrize("inverse", [False, True])
+def test_rope_is_numpys_complex_multiply(inverse):
+    x, rot, pos, d, rd = _rope_case(77)
+    n = x.shape[0]
+    y, y64 = oracle.rope(x, rot, pos, rd, inverse, want_f64=True)
+    xs = oracle.bf16_to_f64(x[:, d - rd:]).reshape(n, rd // 2, 2)
+    w = rot[pos].astype(np.float64)
+    w = w[..., 0] + 1j * w[..., 1]
+    ref = (xs[..., 0] + 1j * xs[..., 1]) * (np.conj(w) if inverse else w)
+    ref = np.stack([ref.real, ref.imag], -1).reshape(n, rd)
+    scale = np.abs(oracle.bf16_to_f64(x)).max()
+    assert np.abs(y64 - ref).max() <= 1e-13 * scale
+    assert (y[:, d - rd:] == oracle.bf16_round(ref)).all()
+    assert (y[:, : d - rd] == x[:, : d - rd]).all()        # the other dims untouched
+    # the rotation keeps each pair's length, times the table entry's
+    r2 = (xs ** 2).sum(-1) * np.abs(w) ** 2
+    assert np.allclose((y64.reshape(n, rd // 2, 2) ** 2).sum(-1), r2, rtol=1e-12, atol=0)
+
+
+def test_rope_special_angles_are_exact():
+    x, rot, pos, d, rd = _rope_case(78)
+    a, b = x[:, d - rd::2], x[:, d - rd + 1::2]
+    neg = lambda t: t ^ np.uint16(0x8000)  # noqa: E731
+    for c, s_, fwd, inv in [(1.0, 0.0, (a, b), (a, b)),            # angle 0: identity
+                            (0.0, 1.0, (neg(b), a), (b, neg(a))),  # pi / 2
+                            (-1.0, 0.0, (neg(a), neg(b)), (neg(a), neg(b)))]:  # pi
+        r = np.zeros_like(rot)
+        r[..., 0], r[..., 1] = c, s_
+        for inverse, (ea, eb) in ((False, fwd), (True, inv)):
+            y = oracle.rope(x, r, pos, rd, inverse)
+            # (a signed zero may come out as +0 where -0 went in: compare values)
+            assert np.array_equal(oracle.bf16_to_f64(y[:, d - rd::2]), oracle.bf16_to_f64(ea))
+            assert np.array_equal(oracle.bf16_to_f64(y[:, d - rd + 1::2]), oracle.bf16_to_f64(eb))
+
+
+def test_rope_inverse_undoes_the_rotation():
+    x, rot, pos, d, rd = _rope_case(79)
+    back = oracle.rope(oracle.rope(x, rot, pos, rd, False), rot, pos, rd, True)
+    xv, bv = oracle.bf16_to_f64(x[:, d - rd:]), oracle.bf16_to_f64(back[:, d - rd:])
+    # two bf16 roundings and the f32 table's |w| != 1: within a few bf16 steps of the pair's size
+    pair = np.sqrt((xv.reshape(-1, rd // 2, 2) ** 2).sum(-1)).repeat(2, -1).reshape(xv.shape)
+    assert (np.abs(bv - xv) <= 2 ** -6 * pair + 1e-30).all()
+
+
+def test_rope_rejects_bad_arguments():
+    x, rot, pos, d, rd = _rope_case(80, n=2)
+    with pytest.raises(ValueError):
+        oracle.rope(x, rot, pos, 63, True)          # odd rope_dim
+    with pytest.raises(ValueError):
+        oracle.rope(x, rot, [0, 50], rd, True)      # a position past the table
