@@ -84,6 +84,38 @@ sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale,
                          int64_t b, int64_t s, int h, int d, int64_t rows, int topk,
                          void* o, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * sparse_attn with the inverse rotary embedding of the output fused in.
+ *
+ * Source: "DeepSeek V4.1" attention page, Attention.forward (after sparse_attn, the last
+ * rope_dim dims of o are rotated back with apply_rotary_emb(..., inverse=True)) and
+ * apply_rotary_emb (pairs of dims as complex numbers, times the position's rotation or its
+ * conjugate); Attention.__init__ (rope_head_dim = 64 of head_dim 512).
+ *
+ * Computes what sa_sparse_attn computes, then, for every sequence bi, token si and head hh,
+ * with p = start_pos + si and k < rope_dim / 2, the pair (a, b) = o[.., d - rope_dim + 2k],
+ * o[.., d - rope_dim + 2k + 1] becomes
+ *   (a c + b s,  b c - a s),   (c, s) = rot[p][k][0], rot[p][k][1]
+ * (a + i b times c - i s).  The rotation is applied to the f32 result before its one rounding
+ * to bf16; the two-step form (o rounded to bf16, rotated, rounded again) differs from it by at
+ * most about one bf16 unit of o.
+ *
+ * Arguments as sa_sparse_attn (same workspace size), plus
+ *   rot        f32 [npos][rope_dim / 2][2] (cos, sin) per position, 8-byte aligned; must not
+ *              overlap o
+ *   npos       positions in rot; start_pos + s <= npos
+ *   rope_dim   even, 2 <= rope_dim <= d
+ *   start_pos  position of token 0 of every sequence (the prefill's 0, a decode step's length)
+ * Supported: d = 512 (the tcgen05 kernel family, which fuses the rotation into its epilogue);
+ * other head dims, or SA_FORCE_MMA=1 in the environment, return SA_ERR_UNSUPPORTED.
+ */
+sa_status sa_sparse_attn_rope(const void* q, const void* kv, const uint8_t* kv_scale,
+                              int kv_format, const float* sink, const int32_t* idx,
+                              float softmax_scale, int64_t b, int64_t s, int h, int d,
+                              int64_t rows, int topk, void* o, void* workspace,
+                              size_t workspace_bytes, const float* rot, int64_t npos, int rope_dim,
+                              int64_t start_pos, void* stream);
+
 /* Workspace bytes sa_sparse_attn needs for this shape (always >= SA_STATUS_BYTES).  Returns 0
  * for an unsupported shape. */
 size_t sa_sparse_attn_workspace_size(int64_t b, int64_t s, int h, int d, int64_t rows, int topk,

@@ -58,11 +58,13 @@ def new_workspace(b, s, h, d, rows, topk, kv_format=SA_KV_BF16, device="cuda") -
 
 
 def sparse_attn(q, kv, sink, idx, softmax_scale, *, kv_scale=None, out=None, workspace=None,
-                stream=None) -> torch.Tensor:
+                rope=None, stream=None) -> torch.Tensor:
     """o[b, s, h, d] (bf16) = sparse_attn(q, kv, sink, idx, softmax_scale).
 
     q [b, s, h, d] bf16; kv [b, rows, d] bf16, or uint8 e4m3 codes with kv_scale [b, rows, d/32]
-    uint8 e8m0; sink [h] f32; idx [b, s, topk] int32 (-1 = empty)."""
+    uint8 e8m0; sink [h] f32; idx [b, s, topk] int32 (-1 = empty).
+    rope=(rot, start_pos): also rotate o's last rot.shape[1] * 2 dims back by the inverse rotary
+    embedding of positions start_pos + si, rot [positions, rope_dim / 2, 2] f32 (cos, sin)."""
     _need(q, "q", torch.bfloat16)
     dev = q.device
     b, s, h, d = q.shape
@@ -92,6 +94,18 @@ def sparse_attn(q, kv, sink, idx, softmax_scale, *, kv_scale=None, out=None, wor
         workspace = new_workspace(b, s, h, d, rows, topk, fmt, device=dev)
     else:
         _need(workspace, "workspace", torch.uint8, dev)
+    if rope is not None:
+        rot, start_pos = rope
+        _need(rot, "rot", torch.float32, dev)
+        if rot.dim() != 3 or rot.shape[2] != 2:
+            raise ValueError(f"rot shape {tuple(rot.shape)} is not [positions, rope_dim / 2, 2]")
+        st = load().sa_sparse_attn_rope(_ptr(q), _ptr(kv), _ptr(kv_scale), fmt, _ptr(sink),
+                                        _ptr(idx), float(softmax_scale), b, s, h, d, rows, topk,
+                                        _ptr(out), _ptr(workspace), workspace.numel(), _ptr(rot),
+                                        rot.shape[0], 2 * rot.shape[1], int(start_pos),
+                                        _stream(stream))
+        _lib.check(st, "sa_sparse_attn_rope")
+        return out
     st = load().sa_sparse_attn(_ptr(q), _ptr(kv), _ptr(kv_scale), fmt, _ptr(sink), _ptr(idx),
                                float(softmax_scale), b, s, h, d, rows, topk, _ptr(out),
                                _ptr(workspace), workspace.numel(), _stream(stream))

@@ -47,6 +47,9 @@ def load() -> ctypes.CDLL:
         lib.sa_sparse_attn.restype = i32
         lib.sa_sparse_attn.argtypes = [P, P, P, i32, P, P, f32, i64, i64, i32, i32, i64, i32, P, P,
                                        sz, P]
+        lib.sa_sparse_attn_rope.restype = i32
+        lib.sa_sparse_attn_rope.argtypes = [P, P, P, i32, P, P, f32, i64, i64, i32, i32, i64, i32,
+                                            P, P, sz, P, i64, i32, i64, P]
         lib.sa_sparse_attn_workspace_size.restype = sz
         lib.sa_sparse_attn_workspace_size.argtypes = [i64, i64, i32, i32, i64, i32, i32]
         lib.sa_window_idxs.restype = i32

@@ -38,6 +38,13 @@ bool force_mma() {
     return v && v[0] == '1';
 }
 
+// The whole sparse_attn call; rope == nullptr for none (checked by the caller).
+sa_status attn_call(const void* q, const void* kv, const uint8_t* kv_scale, int kv_format,
+                    const float* sink, const int32_t* idx, float softmax_scale, int64_t b, int64_t s,
+                    int h, int d, int64_t rows, int topk, void* o, void* workspace,
+                    size_t workspace_bytes, const float* rope, int rope_dim, int64_t rope_pos0,
+                    void* stream);
+
 }  // namespace
 
 extern "C" {
@@ -59,6 +66,39 @@ sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale,
                          const float* sink, const int32_t* idx, float softmax_scale,
                          int64_t b, int64_t s, int h, int d, int64_t rows, int topk,
                          void* o, void* workspace, size_t workspace_bytes, void* stream) {
+    return attn_call(q, kv, kv_scale, kv_format, sink, idx, softmax_scale, b, s, h, d, rows, topk,
+                     o, workspace, workspace_bytes, nullptr, 0, 0, stream);
+}
+
+sa_status sa_sparse_attn_rope(const void* q, const void* kv, const uint8_t* kv_scale,
+                              int kv_format, const float* sink, const int32_t* idx,
+                              float softmax_scale, int64_t b, int64_t s, int h, int d,
+                              int64_t rows, int topk, void* o, void* workspace,
+                              size_t workspace_bytes, const float* rot, int64_t npos, int rope_dim,
+                              int64_t start_pos, void* stream) {
+    if (rope_dim < 2 || rope_dim % 2 != 0 || rope_dim > d || npos < 0 || start_pos < 0)
+        return SA_ERR_INVALID_ARG;
+    if (start_pos > npos - s) return SA_ERR_INVALID_ARG;  // positions start_pos .. start_pos + s - 1
+    if (kv_format != SA_KV_BF16 && kv_format != SA_KV_FP8_E4M3) return SA_ERR_INVALID_ARG;
+    // the rotation is fused into the tcgen05 kernel's epilogue only
+    if (!sa::attn_tc_supports(h, d, kv_format, b, rows) || force_mma()) return SA_ERR_UNSUPPORTED;
+    if (b * s > 0 && (!rot || !aligned(rot, 8))) return SA_ERR_INVALID_ARG;
+    if (b * s > 0 && overlaps(o, (size_t)(b * s) * h * (size_t)d * 2, rot,
+                              (size_t)npos * rope_dim * sizeof(float)))
+        return SA_ERR_INVALID_ARG;
+    return attn_call(q, kv, kv_scale, kv_format, sink, idx, softmax_scale, b, s, h, d, rows, topk,
+                     o, workspace, workspace_bytes, rot, rope_dim, start_pos, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+sa_status attn_call(const void* q, const void* kv, const uint8_t* kv_scale, int kv_format,
+                    const float* sink, const int32_t* idx, float softmax_scale, int64_t b, int64_t s,
+                    int h, int d, int64_t rows, int topk, void* o, void* workspace,
+                    size_t workspace_bytes, const float* rope, int rope_dim, int64_t rope_pos0,
+                    void* stream) {
     if (kv_format != SA_KV_BF16 && kv_format != SA_KV_FP8_E4M3) return SA_ERR_INVALID_ARG;
     if (b < 0 || s < 0 || h < 1 || d < 1 || rows < 0 || topk < 0) return SA_ERR_INVALID_ARG;
     if (!supported_shape(b, s, h, d, rows, topk)) return SA_ERR_UNSUPPORTED;
@@ -101,10 +141,18 @@ sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale,
     c.scratch = reinterpret_cast<uint8_t*>(workspace) + SA_STATUS_BYTES;
     c.scratch_bytes = workspace_bytes - SA_STATUS_BYTES;
     c.stream = reinterpret_cast<cudaStream_t>(stream);
+    c.rope = rope;
+    c.rope_dim = rope_dim;
+    c.rope_pos0 = rope_pos0;
+    if (rope) return from_cuda(sa::attn_tc_launch(c));  // the caller checked the tc family applies
     if (sa::attn_tc_supports(h, d, kv_format, b, rows) && !force_mma())
         return from_cuda(sa::attn_tc_launch(c));
     return from_cuda(sa::attn_mma_launch(c));
 }
+
+}  // namespace
+
+extern "C" {
 
 sa_status sa_window_idxs(int64_t start_pos, int64_t seqlen, int window, int32_t* idx, int64_t ld,
                          int64_t nbatch, int64_t batch_stride, void* stream) {

@@ -138,6 +138,9 @@ struct Params {
     int n_splits;
     int tiles_per_split;  // even when the columns are split, so that pairs never straddle tasks
     int64_t n_units;      // (token, split) units; each is one task per head block
+    const float* rope;    // inverse rotation of o's last rope_dim dims, or nullptr (see AttnCall)
+    int rope_dim;
+    int64_t rope_pos0;
 };
 
 struct Task {
@@ -916,6 +919,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(smem_addr(&M.o_empty[c]));  // the MMA may refill this chunk now
+                if (t.t1 == t.t0) {
+                    // no row tile (topk == 0): no MMA wrote O, and TMEM holds whatever it last
+                    // held, so the result is set to the exact zero of an empty sum
+#pragma unroll
+                    for (int i = 0; i < kHeads; ++i) r[i] = 0u;
+                }
+                if (p.rope != nullptr && 128 * c + 32 * q4 + 32 > kD - p.rope_dim) {
+                    // the inverse rotation of the rope dims ("DeepSeek V4.1" attention page,
+                    // apply_rotary_emb with inverse, on o[..., -rope_dim:]): lanes 2k and 2k + 1
+                    // hold the real and imaginary part of one pair of every head; (a + i b)
+                    // (c - i s) = (a c + b s) + i (b c - a s), on the f32 O before any rounding
+                    // (split partials too: the merge is linear)
+                    const int dd = 128 * c + 32 * q4 + lane, first = kD - p.rope_dim;
+                    const bool mine = dd >= first, odd = (lane & 1) != 0;
+                    float cs = 1.f, sn = 0.f;
+                    if (mine) {
+                        const float2 w = reinterpret_cast<const float2*>(
+                            p.rope)[(p.rope_pos0 + t.pos) * (p.rope_dim / 2) + ((dd - first) >> 1)];
+                        cs = w.x;
+                        sn = w.y;
+                    }
+#pragma unroll
+                    for (int i = 0; i < kHeads; ++i) {
+                        const float v = __uint_as_float(r[i]);
+                        const float u = __shfl_xor_sync(0xffffffffu, v, 1);
+                        const float rv = odd ? fmaf(v, cs, -u * sn) : fmaf(v, cs, u * sn);
+                        r[i] = __float_as_uint(mine ? rv : v);
+                    }
+                }
                 if (split) {
                     if (ok) {
                         float* po = p.part_o + pbase * kD + 128 * c + 32 * q4 + lane;
@@ -1076,6 +1108,9 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
     Params p;
     const bool fp8 = c.kv_format == SA_KV_FP8_E4M3;
     p.q = reinterpret_cast<const __nv_bfloat16*>(c.q);
+    p.rope = c.rope;
+    p.rope_dim = c.rope_dim;
+    p.rope_pos0 = c.rope_pos0;
     p.kv = fp8 ? nullptr : reinterpret_cast<const __nv_bfloat16*>(c.kv);
     p.kv8 = fp8 ? reinterpret_cast<const uint8_t*>(c.kv) : nullptr;
     p.kv_scale = fp8 ? c.kv_scale : nullptr;

@@ -31,6 +31,12 @@ struct AttnCall {
     void* scratch;      // workspace past the status block
     size_t scratch_bytes;
     cudaStream_t stream;
+    // optional inverse rotation of o's last rope_dim dims (apply_rotary_emb, inverse): rope is the
+    // [positions][rope_dim / 2][2] (cos, sin) f32 table, token (bi, si) at position rope_pos0 + si;
+    // nullptr for none
+    const float* rope = nullptr;
+    int rope_dim = 0;
+    int64_t rope_pos0 = 0;
 };
 
 // mma.sync family (sa_attn_mma.cu)

@@ -209,3 +209,11 @@ def make_random(b, s, h, d, rows, topk, *, seed, window=0, start_pos=0, kv_forma
     return Workload(f"random_b{b}_s{s}_h{h}_d{d}_r{rows}_k{topk}", b, s, h, d, rows, topk, window,
                     start_pos, kv_format, float(np.float32(d ** -0.5)), q, sink, tail, drop,
                     kv_rows, kv_vals, seed=seed)
+
+
+def rope_table(npos: int, rope_dim: int, *, seed: int) -> np.ndarray:
+    """A rotation table for the output's rope dims: [npos, rope_dim / 2, 2] f32 (cos, sin) of
+    angles drawn uniformly from [-pi, pi) (the layer's own table holds position times frequency;
+    any angle exercises the rotation the same way), computed by numpy's cos / sin."""
+    ang = np.random.default_rng(seed).uniform(-np.pi, np.pi, (npos, rope_dim // 2))
+    return np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)

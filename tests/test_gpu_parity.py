@@ -12,7 +12,7 @@ import oracle
 import sparse_latent_attention_gb300 as sa
 from sparse_latent_attention_gb300 import build, workloads
 from tests import _gpu
-from tests._helpers import assert_close_bf16, compose_idx_oracle
+from tests._helpers import assert_close_bf16, compose_idx_oracle, quantised_kv_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -254,6 +254,50 @@ def test_random_parity(dev, case):
     assert (_gpu.bf16_tensor_to_u16(o.view(-1, h, d)[1]) == 0).all()
 
 
+ROPE_CASES = [
+    # b, s, h, rows, topk, rope_dim, start_pos, quantise
+    (2, 37, 64, 300, 200, 64, 0, False),        # prefill, the layer's 64 rope dims
+    (3, 1, 64, 5000, 1152, 64, 4000, False),    # decode: split partials rotated, then merged
+    (2, 9, 100, 300, 200, 64, 5, False),        # a partial head block
+    (2, 9, 64, 300, 200, 64, 11, True),         # fp8 kv
+    (1, 12, 64, 200, 130, 512, 3, False),       # the whole head rotated
+    (1, 12, 64, 200, 130, 2, 3, False),         # one pair: the last two dims only
+    (2, 5, 64, 300, 0, 64, 2, False),           # no idx columns: o = 0 stays 0
+]
+
+
+@pytest.mark.parametrize("case", ROPE_CASES,
+                         ids=lambda c: f"b{c[0]}s{c[1]}h{c[2]}k{c[4]}r{c[5]}p{c[6]}{'q' if c[7] else ''}")
+def test_inverse_rope_fused(dev, case):
+    # sparse_attn followed by apply_rotary_emb(o[..., -rope_dim:], inverse) at the positions
+    # start_pos + si ("DeepSeek V4.1" attention page, Attention.forward): the oracle takes the two
+    # steps as the page writes them (o rounded to bf16, then rotated and rounded again); the kernel
+    # rotates its f32 result before its one rounding, within the tolerance of the two-step form.
+    b, s, h, rows, topk, rd, start_pos, quantise = case
+    d = 512
+    wl = workloads.make_random(b, s, h, d, rows, topk, seed=3000 + rd + start_pos,
+                               all_neg_tokens=(1,) if b * s > 1 else (),
+                               kv_format="fp8" if quantise else "bf16")
+    rot = workloads.rope_table(start_pos + s + 3, rd, seed=rd + start_pos)
+    x = _gpu.prepare(wl, dev, quantise)
+    fmt = sa.SA_KV_FP8_E4M3 if x["kv_scale"] is not None else sa.SA_KV_BF16
+    ws = sa.new_workspace(b, s, h, d, wl.rows, wl.topk, fmt, device=dev)
+    plain = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, kv_scale=x["kv_scale"],
+                           workspace=ws)
+    o = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, kv_scale=x["kv_scale"],
+                       workspace=ws, rope=(torch.from_numpy(rot).to(dev), start_pos))
+    torch.cuda.synchronize()
+    assert sa.read_status(ws) == 0
+    # the dims outside the rope slice are the plain call's, bit for bit
+    assert torch.equal(o[..., :d - rd].view(torch.int16), plain[..., :d - rd].view(torch.int16))
+    kv_o = quantised_kv_oracle(wl, quantise)[0]  # fp8 rows decode to the round trip's values
+    o_or = oracle.sparse_attn(wl.q, kv_o, wl.sink, compose_idx_oracle(wl), wl.scale)
+    o_or = o_or.reshape(b * s * h, d)
+    pos = np.repeat(np.tile(start_pos + np.arange(s), b), h)
+    want = oracle.rope(o_or, rot, pos, rd, True).reshape(b, s, h, d)
+    assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what=str(case))
+
+
 def test_running_max_raised_every_tile(dev):
     # The logits grow by ~7 nats (> 2^8 in log2 units) from one block of 64 rows to the next, so
     # a token that lists the rows in order raises its running maximum (and rescales O) on every
@@ -324,7 +368,7 @@ def test_empty_shapes(dev):
         sink = torch.from_numpy(wl.sink).to(dev)
         o = torch.full_like(q, 3.0)
         sa.sparse_attn(q, kv, sink, idx, wl.scale, out=o)
-        assert (o == 0).all()
+        assert (o.view(torch.int16) == 0).all()  # +0 bit patterns, whatever TMEM held before
     # no tokens at all: a no-op
     q = torch.empty((0, 4, 64, 512), dtype=torch.bfloat16, device=dev)
     o = sa.sparse_attn(q, torch.zeros((0, 5, 512), dtype=torch.bfloat16, device=dev),

@@ -20,7 +20,8 @@ def test_exports_every_declared_symbol(lib):
     names = _lib.declared_symbols()
     assert set(names) == {"sa_sparse_attn", "sa_sparse_attn_workspace_size", "sa_window_idxs",
                           "sa_act_quant_fp8", "sa_read_status", "sa_status_string", "sa_version",
-                          "sa_sparse_attn_static_scratch", "sa_window_write"}
+                          "sa_sparse_attn_static_scratch", "sa_window_write",
+                          "sa_sparse_attn_rope"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -73,6 +74,40 @@ def _attn(lib, **kw):
 ])
 def test_sparse_attn_rejects_bad_arguments(lib, kw, code):
     assert _attn(lib, **kw) == code
+
+
+def _attn_rope(lib, **kw):
+    a = dict(q=FAKE, kv=FAKE, kv_scale=None, fmt=0, sink=FAKE, idx=FAKE, scale=0.1, b=1, s=2,
+             h=64, d=512, rows=8, topk=4, o=ctypes.c_void_p((1 << 40) + (1 << 30)), ws=None,
+             ws_bytes=0, rot=FAKE2, npos=16, rope_dim=64, start_pos=3, stream=None)
+    a.update(kw)
+    return lib.sa_sparse_attn_rope(a["q"], a["kv"], a["kv_scale"], a["fmt"], a["sink"], a["idx"],
+                                   a["scale"], a["b"], a["s"], a["h"], a["d"], a["rows"],
+                                   a["topk"], a["o"], a["ws"], a["ws_bytes"], a["rot"], a["npos"],
+                                   a["rope_dim"], a["start_pos"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), _lib.SA_ERR_WORKSPACE),                    # valid rotation: the shared checks follow
+    (dict(rope_dim=63), _lib.SA_ERR_INVALID_ARG),       # odd
+    (dict(rope_dim=0), _lib.SA_ERR_INVALID_ARG),
+    (dict(rope_dim=514), _lib.SA_ERR_INVALID_ARG),      # wider than the head
+    (dict(start_pos=15), _lib.SA_ERR_INVALID_ARG),      # positions 15, 16 past a 16-row table
+    (dict(start_pos=-1), _lib.SA_ERR_INVALID_ARG),
+    (dict(npos=-1), _lib.SA_ERR_INVALID_ARG),
+    (dict(d=256, rope_dim=64), _lib.SA_ERR_UNSUPPORTED),  # only the d = 512 kernel fuses it
+    (dict(rot=None), _lib.SA_ERR_INVALID_ARG),
+    (dict(rot=ctypes.c_void_p((1 << 41) + 4)), _lib.SA_ERR_INVALID_ARG),  # not 8-byte aligned
+    (dict(rot=ctypes.c_void_p((1 << 40) + (1 << 30) + 256)), _lib.SA_ERR_INVALID_ARG),  # in o
+    (dict(rot=None, b=0), _lib.SA_OK),                  # no tokens: nothing is read
+])
+def test_sparse_attn_rope_rejects_bad_arguments(lib, kw, code):
+    assert _attn_rope(lib, **kw) == code
+
+
+def test_sparse_attn_rope_unsupported_on_forced_mma(lib, monkeypatch):
+    monkeypatch.setenv("SA_FORCE_MMA", "1")
+    assert _attn_rope(lib) == _lib.SA_ERR_UNSUPPORTED
 
 
 def test_window_idxs_rejects_bad_arguments(lib):
