@@ -50,9 +50,9 @@ L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 # from the ncu captures summarised under profiles/, keyed by (hash of the CUDA sources the capture
 # ran, workload).  Any change to the sources makes the key miss, so a stale figure reads as null.
 NCU_TRAFFIC = {
-    ("809a7d6c2a3e885c", "swa_prefill"): 500_622_848,
-    ("809a7d6c2a3e885c", "cmp_prefill"): 1_066_425_088,
-    ("809a7d6c2a3e885c", "decode"): 82_903_552,
+    ("42e9fade7067edd6", "swa_prefill"): 500_602_112,
+    ("42e9fade7067edd6", "cmp_prefill"): 1_066_232_064,
+    ("42e9fade7067edd6", "decode"): 83_038_720,
 }
 
 
@@ -232,7 +232,7 @@ def roofline_terms(wl, idx_np, peaks):
 class GpuPath:
     """Device buffers of one workload and its step through the library."""
 
-    def __init__(self, wl, dev):
+    def __init__(self, wl, dev, rope_dim=0):
         import torch
 
         import sparse_latent_attention_gb300 as sa
@@ -272,6 +272,11 @@ class GpuPath:
         self.ws = sa.new_workspace(wl.b, wl.s, wl.h, d, wl.rows, wl.topk,
                                    sa.SA_KV_FP8_E4M3 if self.fp8 else sa.SA_KV_BF16, device=dev)
         self.launches_per_step = 2 + (2 if self.ws.numel() > sa.SA_STATUS_BYTES else 1)
+        # optional inverse rotation of o's last rope_dim dims, fused into the attention call
+        self.rot = None
+        if rope_dim:
+            self.rot = torch.from_numpy(
+                workloads.rope_table(wl.start_pos + wl.s, rope_dim, seed=7)).to(dev)
 
     def step(self, ev=None):
         """One pass of the path; ev = (start, end) CUDA events bracketing sparse_attn."""
@@ -296,9 +301,14 @@ class GpuPath:
         """sparse_attn over every query, or over one part from chunks() (on the current stream)."""
         wl = self.wl
         qs, ks = part if part is not None else ((slice(None),), (slice(None),))
+        rope = None
+        if self.rot is not None:  # a part of a prefill starts at its first token's position
+            first = (qs[1].start or 0) if len(qs) > 1 else 0
+            rope = (self.rot, wl.start_pos + first)
         self.sa.sparse_attn(self.q[qs], self.kv[ks], self.sink, self.idx[qs], wl.scale,
                             kv_scale=None if self.kv_scale is None else self.kv_scale[ks],
-                            out=self.o[qs], workspace=self.ws if workspace is None else workspace)
+                            out=self.o[qs], workspace=self.ws if workspace is None else workspace,
+                            rope=rope)
 
     def workspace_for(self, parts):
         """A workspace large enough for every part (fewer queries can mean more split scratch)."""
@@ -333,7 +343,7 @@ def run_gpu(args, rank, world, local):
     rank0 = rank == 0
     peaks = load_peaks()
     wl = workloads.make_named(args.workload, batch=args.batch)
-    path = GpuPath(wl, dev)
+    path = GpuPath(wl, dev, rope_dim=args.rope)
     path.step()
     torch.cuda.synchronize()
     idx_np = path.idx.cpu().numpy()
@@ -476,7 +486,8 @@ def run_gpu(args, rank, world, local):
                    "rows": wl.rows, "topk": wl.topk, "window": wl.window,
                    "start_pos": wl.start_pos, "kv_format": wl.kv_format,
                    "l2": "flushed between timed steps (256 MB write, outside the step events)",
-                   "parallelism": f"replica x{world}" if world > 1 else "1 GPU"},
+                   "parallelism": f"replica x{world}" if world > 1 else "1 GPU",
+                   **({"inverse_rope_dims": args.rope} if args.rope else {})},
         "roofline": roof,
         "e2e": {"value": round(job_value(units, world, ms_e2e / 1e3), 1), "unit": UNIT,
                 "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": int(h2d),
@@ -646,6 +657,9 @@ def main(argv=None):
     ap.add_argument("--e2e-chunks", type=int, default=0,
                     help="parts the end-to-end step's queries are copied and attended in "
                          "(0: one per 256 query tokens, at most 16)")
+    ap.add_argument("--rope", type=int, default=0, metavar="DIMS",
+                    help="also rotate o's last DIMS dims back (inverse RoPE fused into the call; "
+                         "the layer uses 64); 0 = off")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -274,7 +274,9 @@ __device__ __forceinline__ void widen_fp8(uint32_t s_kv, const Misc& M, const in
     }
 }
 
-template <bool kFp8>
+// kRope: the inverse rotation of o's rope dims is fused into the epilogue (a separate
+// instantiation, so that the plain kernel carries none of its code)
+template <bool kFp8, bool kRope>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap o_map,
                    Params p) {
@@ -919,13 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(smem_addr(&M.o_empty[c]));  // the MMA may refill this chunk now
-                if (t.t1 == t.t0) {
-                    // no row tile (topk == 0): no MMA wrote O, and TMEM holds whatever it last
-                    // held, so the result is set to the exact zero of an empty sum
-#pragma unroll
-                    for (int i = 0; i < kHeads; ++i) r[i] = 0u;
-                }
-                if (p.rope != nullptr && 128 * c + 32 * q4 + 32 > kD - p.rope_dim) {
+                if (kRope && 128 * c + 32 * q4 + 32 > kD - p.rope_dim) {
                     // the inverse rotation of the rope dims ("DeepSeek V4.1" attention page,
                     // apply_rotary_emb with inverse, on o[..., -rope_dim:]): lanes 2k and 2k + 1
                     // hold the real and imaginary part of one pair of every head; (a + i b)
@@ -1081,6 +1077,8 @@ size_t attn_tc_scratch_bytes(int64_t b, int64_t s, int h, int topk) {
 
 cudaError_t attn_tc_launch(const AttnCall& c) {
     const int64_t n_tokens = c.b * c.s;
+    if (c.topk == 0)  // no row at all: o is the zero of an empty sum (rotated or not)
+        return cudaMemsetAsync(c.o, 0, (size_t)n_tokens * c.h * kD * 2, c.stream);
     const TcGeometry g = tc_geometry(n_tokens, c.h, c.topk);
     auto encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
@@ -1141,22 +1139,24 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_tc_kernel<true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
+        void (*const fns[4])(const CUtensorMap, const CUtensorMap, Params) = {
+            attn_tc_kernel<false, false>, attn_tc_kernel<true, false>, attn_tc_kernel<false, true>,
+            attn_tc_kernel<true, true>};
+        for (auto fn : fns) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
+            if (e != cudaSuccess) return e;
+        }
         if (dev < 64) configured[dev] = true;
     }
     int64_t groups = sm_count() / g.hblocks;  // CTA groups, one CTA per head block
     if (groups > p.n_units) groups = p.n_units;
     if (groups < 1) groups = 1;
     const int64_t grid = groups * g.hblocks;
-    if (fp8)
-        attn_tc_kernel<true><<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
-    else
-        attn_tc_kernel<false><<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
+    const bool rope = c.rope != nullptr;
+    auto kernel = fp8 ? (rope ? attn_tc_kernel<true, true> : attn_tc_kernel<true, false>)
+                      : (rope ? attn_tc_kernel<false, true> : attn_tc_kernel<false, false>);
+    kernel<<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || g.n_splits == 1) return e;
     return attn_combine_launch(p.part_ml, p.part_o, c.sink, c.o, n_tokens, c.h, kD, g.n_splits,
