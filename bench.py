@@ -8,7 +8,7 @@ A step is one pass of the whole path over one batch of synthetic input:
   3. sparse_attn   -- the index-gathered attention with the sink
 The metric is query-heads per second (b * s * h per step time).  `value` is device time with
 inputs resident in HBM (L2 flushed between steps, each step timed with CUDA events on the
-launching stream); `e2e` times the same step through the public API with the step's inputs
+launching stream, and queued whole before its first event fires); `e2e` times the same step through the public API with the step's inputs
 copied from pinned host memory and the output read back, the queries in parts (--e2e-chunks)
 whose copies in and out overlap the attention of other parts.  `roofline` relates the sparse_attn
 launch to the binding roofline (HBM bytes or dense bf16 FLOPs), and `cpu_baseline` times the CPU
@@ -45,14 +45,18 @@ UNIT = "query·heads/s"
 DEFAULT_WORKLOAD = "swa_prefill"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+# A GPU-side spin (~0.2 ms at 2 GHz) after each flush, before the step's first event: the host
+# enqueues the whole step while the GPU spins, so the events time the step's kernels back to back
+# and not the host's argument marshalling between them (the e2e figure keeps the host in).
+HEAD_START_CYCLES = 400_000
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel (attn_tc_kernel),
 # from the ncu captures summarised under profiles/, keyed by (hash of the CUDA sources the capture
 # ran, workload).  Any change to the sources makes the key miss, so a stale figure reads as null.
 NCU_TRAFFIC = {
-    ("42e9fade7067edd6", "swa_prefill"): 500_602_112,
-    ("42e9fade7067edd6", "cmp_prefill"): 1_066_232_064,
-    ("42e9fade7067edd6", "decode"): 83_038_720,
+    ("c32c3a5f1c9cf914", "swa_prefill"): 500_166_656,
+    ("c32c3a5f1c9cf914", "cmp_prefill"): 1_066_483_456,
+    ("c32c3a5f1c9cf914", "decode"): 82_971_648,
 }
 
 
@@ -353,6 +357,7 @@ def run_gpu(args, rank, world, local):
     sampler = ClockSampler(gpu_id_of(torch, dev)).start() if rank0 else None
     for _ in range(args.warmup):
         flush.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)
         path.step()
     torch.cuda.synchronize()
 
@@ -365,6 +370,7 @@ def run_gpu(args, rank, world, local):
     t0 = time.time()
     for e in ev:
         flush.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)  # not timed: lets the host queue the step first
         e[0].record()
         path.step(ev=(e[2], e[3]))
         e[1].record()
@@ -486,6 +492,8 @@ def run_gpu(args, rank, world, local):
                    "rows": wl.rows, "topk": wl.topk, "window": wl.window,
                    "start_pos": wl.start_pos, "kv_format": wl.kv_format,
                    "l2": "flushed between timed steps (256 MB write, outside the step events)",
+                   "launch": "each step fully queued before its first event (a 0.2 ms GPU spin "
+                             "after the flush, outside the events)",
                    "parallelism": f"replica x{world}" if world > 1 else "1 GPU",
                    **({"inverse_rope_dims": args.rope} if args.rope else {})},
         "roofline": roof,

@@ -851,6 +851,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kpar = (int)(k & 1);
             const int h0 = t.hb * kHeads;
             const int hc = min(kHeads, p.h - h0);
+            // the cos / sin of this thread's pair in the last O chunk (where the rope dims sit),
+            // loaded now so that the load's latency hides behind the wait for O
+            float2 rope_last = make_float2(1.f, 0.f);
+            if constexpr (kRope) {
+                const int dd = 128 * (kChunks - 1) + 32 * q4 + lane, first = kD - p.rope_dim;
+                if (dd >= first)
+                    rope_last = reinterpret_cast<const float2*>(
+                        p.rope)[(p.rope_pos0 + t.pos) * (p.rope_dim / 2) + ((dd - first) >> 1)];
+            }
             if constexpr (kFp8) {
                 // widen every tile the producers have staged until this task's O is complete
                 // (its last tile needs this warpgroup's widening first); the poll is bounded
@@ -929,13 +938,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // (split partials too: the merge is linear)
                     const int dd = 128 * c + 32 * q4 + lane, first = kD - p.rope_dim;
                     const bool mine = dd >= first, odd = (lane & 1) != 0;
-                    float cs = 1.f, sn = 0.f;
-                    if (mine) {
-                        const float2 w = reinterpret_cast<const float2*>(
+                    float2 w = rope_last;  // the last chunk's pair was loaded before the wait
+                    if (c != kChunks - 1 && mine)
+                        w = reinterpret_cast<const float2*>(
                             p.rope)[(p.rope_pos0 + t.pos) * (p.rope_dim / 2) + ((dd - first) >> 1)];
-                        cs = w.x;
-                        sn = w.y;
-                    }
+                    const float cs = w.x, sn = w.y;
 #pragma unroll
                     for (int i = 0; i < kHeads; ++i) {
                         const float v = __uint_as_float(r[i]);
