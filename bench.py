@@ -51,27 +51,49 @@ L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 HEAD_START_CYCLES = 400_000
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel (attn_tc_kernel),
-# from the ncu captures summarised under profiles/, keyed by (hash of the CUDA sources the capture
-# ran, workload).  Any change to the sources makes the key miss, so a stale figure reads as null.
+# from the ncu captures summarised under profiles/, keyed by (hash of the files the attention
+# kernels are compiled from, workload).  Any change to those files makes the key miss, so a stale
+# figure reads as null.
 NCU_TRAFFIC = {
-    ("c32c3a5f1c9cf914", "swa_prefill"): 500_166_656,
-    ("c32c3a5f1c9cf914", "cmp_prefill"): 1_066_483_456,
-    ("c32c3a5f1c9cf914", "decode"): 82_971_648,
+    ("ea7a20fce0aa8291", "swa_prefill"): 500_166_656,
+    ("ea7a20fce0aa8291", "cmp_prefill"): 1_066_483_456,
+    ("ea7a20fce0aa8291", "decode"): 82_971_648,
 }
 
 
-def kernel_source_hash() -> str:
-    """First 16 hex digits of the sha256 over the library's CUDA sources (name + bytes, sorted)."""
-    import glob
+# The translation units of the attention kernels (attn_tc_kernel, attn_mma_kernel and the split
+# merge) and every header they include.
+ATTN_SOURCES = ("sparse_latent_attention_gb300/csrc/sa_attn_tc.cu",
+                "sparse_latent_attention_gb300/csrc/sa_attn_mma.cu",
+                "sparse_latent_attention_gb300/csrc/sa_tc.cuh",
+                "sparse_latent_attention_gb300/csrc/sa_fp8.cuh",
+                "sparse_latent_attention_gb300/csrc/sa_internal.cuh",
+                "include/sparse_attn.h")
+
+
+def _sha16(paths) -> str:
     import hashlib
-    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "sparse_latent_attention_gb300",
-                        "csrc")
+    root = os.path.dirname(os.path.abspath(__file__))
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for rel in sorted(paths):
+        h.update(os.path.basename(rel).encode())
+        with open(os.path.join(root, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the sha256 over the attention kernels' sources (name + bytes)."""
+    return _sha16(ATTN_SOURCES)
+
+
+def library_source_hash() -> str:
+    """The same over every CUDA source and header of the library."""
+    import glob
+    root = os.path.dirname(os.path.abspath(__file__))
+    files = glob.glob(os.path.join(root, "sparse_latent_attention_gb300", "csrc", "*")) + glob.glob(
+        os.path.join(root, "include", "*.h"))
+    return _sha16([os.path.relpath(f, root) for f in files])
 
 
 # --------------------------------------------------------------------------------------------
@@ -504,6 +526,7 @@ def run_gpu(args, rank, world, local):
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "lib_version": lib_version,
         "kernel_source_hash": src_hash,
+        "library_source_hash": library_source_hash(),
     }
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)

@@ -8,7 +8,8 @@ first use and marshals numpy arrays through ctypes.
 
 Sources (see the header of ``sa_oracle.c``): the "Module attn" API page of the spark_model
 deepseek_v41_ref docs (precision paragraph, ring-cache paragraph, act_quant_inplace, pow2_ceil,
-sparse_attn, window_topk_idxs) and the "DeepSeek V4.1" Attention.forward / __init__ pages.
+sparse_attn, window_topk_idxs) and the "DeepSeek V4.1" Attention.forward / __init__ pages
+(Indexer.forward for the selection of the compressed idx).
 """
 
 from __future__ import annotations
@@ -66,6 +67,8 @@ def _load():
             lib.or_rope.argtypes = [P, i64, i64, i64, P, i64, P, ctypes.c_int, P]
             lib.or_ring_write.restype = ctypes.c_int
             lib.or_ring_write.argtypes = [P, P, i64, i64, i64, i64]
+            lib.or_indexer_topk.restype = ctypes.c_int
+            lib.or_indexer_topk.argtypes = [P, i64, i64, i64, i64, i64, i64, i64, P]
             for name in ("or_bf16_round_array", "or_e4m3_encode_array", "or_e4m3_decode_array",
                          "or_pow2_ceil_array"):
                 getattr(lib, name).restype = None
@@ -155,6 +158,25 @@ def window_idxs(start_pos: int, seqlen: int, window: int) -> np.ndarray:
         raise NotImplementedError("chunked prefill (start_pos > 0 and seqlen > 1)")
     if rc != OK:
         raise ValueError(f"or_window_idxs failed ({rc})")
+    return out
+
+
+def indexer_topk(score, start_pos: int, ratio: int, index_topk: int, offset: int) -> np.ndarray:
+    """The indexer's selection on score [b, s, n_comp] (f32, or bf16 bits as uint16, widened
+    exactly): idx [b, s, min(index_topk, n_comp)] int32 (see or_indexer_topk)."""
+    lib = _load()
+    score = np.asarray(score)
+    if score.dtype == np.uint16:
+        score = (score.astype(np.uint32) << 16).view(np.float32)
+    sc = _c(score, np.float32)
+    b, s, n = sc.shape
+    k = min(index_topk, n)
+    out = np.empty((b, s, k), np.int32)
+    rc = lib.or_indexer_topk(_ptr(sc), b, s, n, start_pos, ratio, index_topk, offset, _ptr(out))
+    if rc == UNSUPPORTED:
+        raise NotImplementedError("chunked prefill (start_pos > 0 and seqlen > 1)")
+    if rc != OK:
+        raise ValueError(f"or_indexer_topk failed ({rc})")
     return out
 
 

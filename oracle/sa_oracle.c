@@ -12,6 +12,8 @@
  *   [FWD]  "DeepSeek V4.1" attention page (attention/output, prefill): Attention.forward and
  *          Attention.__init__ (softmax_scale = head_dim ** -0.5, attn_sink per local head),
  *          apply_rotary_emb (the inverse rotation of the output's rope dims).
+ *   [IDX]  the same page, Indexer.forward: the selection that turns index scores into the
+ *          compressed idx (visibility mask, top-k, position sort, -1 / offset).
  *
  * Floating point: dot products, the softmax and the weighted sum are carried in f64; the only
  * rounding to a narrow type is the final bf16 round-to-nearest-even of o.  The act_quant steps
@@ -430,4 +432,72 @@ void or_e4m3_decode_array(const uint8_t* c, double* out, int64_t n) {
 
 void or_pow2_ceil_array(const float* x, float* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = or_pow2_ceil(x[i]);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* [IDX] the indexer's selection                                                              */
+/* ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+    double v;
+    int64_t pos;
+} scored_pos;
+
+/* higher score first; among equal scores the lower position first (the reading taken for the
+ * page's topk, which leaves the order of ties open); -0 and +0 compare equal */
+static int by_score_then_pos(const void* a, const void* b) {
+    const scored_pos* x = (const scored_pos*)a;
+    const scored_pos* y = (const scored_pos*)b;
+    if (x->v > y->v) return -1;
+    if (x->v < y->v) return 1;
+    return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+static int by_value(const void* a, const void* b) {
+    const int64_t x = *(const int64_t*)a, y = *(const int64_t*)b;
+    return (x > y) - (x < y);
+}
+
+/* [IDX] For every sequence bi and query si, over the n_comp = (start_pos + s) / ratio compressed
+ * positions of score [b][s][n_comp]:
+ *   visible = (si + 1) / ratio at a prefill (start_pos == 0), where every position t >= visible
+ *             has its score replaced by -inf; n_comp at a decode step (no mask)
+ *   k       = min(index_topk, n_comp)
+ *   pick the k highest scores, sort the picked positions ascending, and write each as
+ *   t + offset when t < visible, else -1, to idx [b][s][k].
+ * Returns 1 on a bad argument, 2 for a chunked prefill (start_pos > 0 with s > 1), which the
+ * page does not describe. */
+int or_indexer_topk(const float* score, int64_t b, int64_t s, int64_t n_comp, int64_t start_pos,
+                    int64_t ratio, int64_t index_topk, int64_t offset, int32_t* idx) {
+    if (b < 0 || s < 0 || start_pos < 0 || ratio < 1 || index_topk < 0) return 1;
+    if ((start_pos + s) / ratio != n_comp) return 1;
+    if (start_pos > 0 && s > 1) return 2;
+    const int64_t k = index_topk < n_comp ? index_topk : n_comp;
+    if (b * s == 0 || k == 0) return 0;
+    scored_pos* all = (scored_pos*)malloc((size_t)n_comp * sizeof *all);
+    int64_t* pick = (int64_t*)malloc((size_t)k * sizeof *pick);
+    if (!all || !pick) {
+        free(all);
+        free(pick);
+        return 1;
+    }
+    for (int64_t bi = 0; bi < b; ++bi) {
+        for (int64_t si = 0; si < s; ++si) {
+            const float* row = score + (bi * s + si) * n_comp;
+            const int64_t visible = start_pos == 0 ? (si + 1) / ratio : n_comp;
+            for (int64_t t = 0; t < n_comp; ++t) {
+                all[t].v = (start_pos == 0 && t >= visible) ? -INFINITY : (double)row[t];
+                all[t].pos = t;
+            }
+            qsort(all, (size_t)n_comp, sizeof *all, by_score_then_pos);
+            for (int64_t j = 0; j < k; ++j) pick[j] = all[j].pos;
+            qsort(pick, (size_t)k, sizeof *pick, by_value);
+            int32_t* out = idx + (bi * s + si) * k;
+            for (int64_t j = 0; j < k; ++j)
+                out[j] = pick[j] < visible ? (int32_t)(pick[j] + offset) : -1;
+        }
+    }
+    free(all);
+    free(pick);
+    return 0;
 }

@@ -3,6 +3,7 @@ brute force and the pages' worked examples.  No GPU needed."""
 
 from __future__ import annotations
 
+import itertools
 import os
 
 import numpy as np
@@ -462,3 +463,101 @@ def test_rope_rejects_bad_arguments():
         oracle.rope(x, rot, pos, 63, True)          # odd rope_dim
     with pytest.raises(ValueError):
         oracle.rope(x, rot, [0, 50], rd, True)      # a position past the table
+
+
+# --------------------------------------------------------------------------------------------
+# the indexer's selection ("DeepSeek V4.1" attention page, Indexer.forward)
+# --------------------------------------------------------------------------------------------
+
+def _golden_indexer():
+    g = {}
+    for line in open(os.path.join(GOLDEN, "indexer_topk_example.txt")):
+        line = line.split("#")[0].strip()
+        if line:
+            k, _kind, *vals = line.split()
+            g[k] = [float(v) for v in vals]
+    return g
+
+
+def test_indexer_topk_worked_example():
+    g = _golden_indexer()
+    ratio, k, off = int(g["ratio"][0]), int(g["index_topk"][0]), int(g["offset"][0])
+    sc = np.tile(np.array(g["scores"], np.float32), (1, 12, 1))
+    got = oracle.indexer_topk(sc, 0, ratio, k, off)[0]
+    for q in (0, 2, 3, 6, 7, 10, 11):
+        assert got[q].tolist() == [int(v) for v in g[f"prefill_q{q}"]], q
+    dec = oracle.indexer_topk(sc[:, :1], 12, ratio, k, off)[0, 0]
+    assert dec.tolist() == [int(v) for v in g["decode12"]]
+    ties = oracle.indexer_topk(np.ones((1, 1, 4), np.float32), 15, ratio, k, off)[0, 0]
+    assert ties.tolist() == [int(v) for v in g["decode_ties"]]
+
+
+def test_indexer_topk_is_torch_topk_on_distinct_scores():
+    # without ties the picked set is unique: torch.topk (a library routine) on the masked scores,
+    # sorted, gives the same rows
+    rng = np.random.default_rng(91)
+    for b, s, start, ratio, topk in ((2, 64, 0, 4, 5), (3, 1, 1023, 4, 64), (1, 33, 0, 1, 40)):
+        n = (start + s) // ratio
+        sc = rng.permutation(b * s * n).reshape(b, s, n).astype(np.float32) / 7.0  # distinct
+        got = oracle.indexer_topk(sc, start, ratio, topk, 1000)
+        t = torch.from_numpy(sc.astype(np.float64))
+        vis = torch.full((s, 1), n) if start else (torch.arange(1, s + 1) // ratio)[:, None]
+        t = t.masked_fill(torch.arange(n)[None, :] >= vis, float("-inf"))
+        k = min(topk, n)
+        for bi in range(b):
+            for si in range(s):
+                nv = int(vis[si, 0])
+                # finite picks are unique; -inf picks (masked) all become -1
+                want = sorted(torch.topk(t[bi, si], min(k, nv)).indices.tolist())
+                row = [p + 1000 for p in want] + [-1] * (k - len(want))
+                assert got[bi, si].tolist() == row, (b, s, bi, si)
+
+
+def test_indexer_topk_brute_force_with_ties():
+    # every k-subset on tiny rows with heavy ties: the picked set is the one that beats every
+    # other position it leaves out (higher score, or equal score at a lower position)
+    rng = np.random.default_rng(92)
+    for trial in range(200):
+        n = int(rng.integers(1, 8))
+        k = int(rng.integers(0, 9))
+        sc = rng.integers(-2, 3, size=(1, 1, n)).astype(np.float32)
+        sc[sc == -2] = -np.inf
+        if trial % 3 == 0:
+            sc[sc == 0] = -0.0  # -0 ties with +0
+        got = oracle.indexer_topk(sc, 4 * n, 4, k, 10)[0, 0]
+        kk = min(k, n)
+        best = None
+        for S in itertools.combinations(range(n), kk):
+            out = set(range(n)) - set(S)
+            if all(sc[0, 0, i] > sc[0, 0, j] or (sc[0, 0, i] == sc[0, 0, j] and i < j)
+                   for i in S for j in out):
+                assert best is None  # the rule picks exactly one subset
+                best = S
+        assert got.tolist() == [p + 10 for p in best], (sc, k)
+
+
+def test_indexer_topk_row_shape_invariants():
+    rng = np.random.default_rng(93)
+    s, ratio, topk = 200, 4, 16
+    n = s // ratio
+    sc = rng.standard_normal((2, s, n)).astype(np.float32)
+    got = oracle.indexer_topk(sc, 0, ratio, topk, 7)
+    for bi in range(2):
+        for si in range(s):
+            row = got[bi, si]
+            valid = row[row >= 0]
+            assert len(valid) == min(topk, (si + 1) // ratio)        # every visible pick kept
+            assert (row[len(valid):] == -1).all()                    # -1 only at the tail
+            assert (np.diff(valid) > 0).all() and (valid < 7 + (si + 1) // ratio).all()
+
+
+def test_indexer_topk_bf16_scores_and_bad_arguments():
+    rng = np.random.default_rng(94)
+    x = rng.standard_normal((1, 1, 50)).astype(np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)               # truncated to bf16
+    wid = (bits.astype(np.uint32) << 16).view(np.float32)
+    assert (oracle.indexer_topk(bits, 200, 4, 9, 0) == oracle.indexer_topk(wid, 200, 4, 9, 0)).all()
+    with pytest.raises(ValueError):
+        oracle.indexer_topk(x, 0, 4, 9, 0)                           # 50 != (0 + 1) // 4
+    with pytest.raises(NotImplementedError):
+        oracle.indexer_topk(np.zeros((1, 2, 50), np.float32), 99, 2, 9, 0)  # chunked prefill
