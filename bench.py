@@ -362,6 +362,59 @@ class GpuPath:
             sa.act_quant_fp8(nr, out_rt=self.kv[:, : wl.s, :].reshape(-1, d))
 
 
+COMPRESS_RATIO = 4  # the compressed workloads' ratio
+
+
+def time_indexer_topk(wl, dev, steps, warmup, peaks):
+    """The indexer's selection (sa_indexer_topk) at this workload's compressed shape: index scores
+    [b, s, n_comp] f32 drawn N(0, 1), n_comp = (start_pos + s) / 4, -> the workload's compressed
+    idx columns (index_topk = its non-window columns, offset = the rows before the compressed
+    ones).  Timed alone like the step: L2 flushed, the call queued before its events."""
+    import torch
+
+    import sparse_latent_attention_gb300 as sa
+    n = (wl.start_pos + wl.s) // COMPRESS_RATIO
+    index_topk = wl.topk - wl.window
+    if index_topk <= 0 or n == 0 or wl.rows < n:
+        return None  # no compressed columns in this workload
+    offset = wl.rows - n
+    k = min(index_topk, n)
+    g = torch.Generator(device=dev).manual_seed(11)
+    score = torch.randn((wl.b, wl.s, n), generator=g, device=dev, dtype=torch.float32)
+    out = torch.empty((wl.b, wl.s, k), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call():
+        sa.indexer_topk(score, wl.start_pos, COMPRESS_RATIO, index_topk, offset, out=out)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    # algorithmic bytes: the scores a query can see (a prefill's hidden positions are never read)
+    # and the idx written
+    if wl.start_pos == 0:
+        seen = wl.b * sum((si + 1) // COMPRESS_RATIO for si in range(wl.s))
+    else:
+        seen = wl.b * wl.s * n
+    alg = 4 * seen + 4 * wl.b * wl.s * k
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"kernel": "indexer_topk_kernel", "ms": round(ms, 4), "alg_bytes": int(alg),
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "queries": wl.b * wl.s, "positions": n,
+            "k": k, "score": "f32"}
+
+
 def run_gpu(args, rank, world, local):
     import torch
     torch.cuda.set_device(local)
@@ -528,6 +581,9 @@ def run_gpu(args, rank, world, local):
         "kernel_source_hash": src_hash,
         "library_source_hash": library_source_hash(),
     }
+    if args.indexer_topk:
+        out["next_rows"] = {"indexer_topk": time_indexer_topk(wl, dev, args.steps, args.warmup,
+                                                              peaks)}
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     return out
@@ -688,6 +744,8 @@ def main(argv=None):
     ap.add_argument("--e2e-chunks", type=int, default=0,
                     help="parts the end-to-end step's queries are copied and attended in "
                          "(0: one per 256 query tokens, at most 16)")
+    ap.add_argument("--indexer-topk", action="store_true",
+                    help="also time the indexer's selection at the workload's compressed shape")
     ap.add_argument("--rope", type=int, default=0, metavar="DIMS",
                     help="also rotate o's last DIMS dims back (inverse RoPE fused into the call; "
                          "the layer uses 64); 0 = off")

@@ -17,11 +17,12 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (SA_KV_BF16, SA_KV_FP8_E4M3, SA_STATUS_BYTES, SparseAttnError, load,
-                   status_string)
+from ._lib import (SA_KV_BF16, SA_KV_FP8_E4M3, SA_SCORE_BF16, SA_SCORE_F32, SA_STATUS_BYTES,
+                   SparseAttnError, load, status_string)
 
-__all__ = ["sparse_attn", "window_idxs", "act_quant_fp8", "workspace_size", "new_workspace",
-           "read_status", "SparseAttnError", "SA_KV_BF16", "SA_KV_FP8_E4M3", "load"]
+__all__ = ["sparse_attn", "window_idxs", "act_quant_fp8", "window_write", "indexer_topk",
+           "workspace_size", "new_workspace", "read_status", "SparseAttnError", "SA_KV_BF16",
+           "SA_KV_FP8_E4M3", "SA_SCORE_F32", "SA_SCORE_BF16", "load"]
 
 
 def _ptr(t) -> ctypes.c_void_p | None:
@@ -110,6 +111,38 @@ def sparse_attn(q, kv, sink, idx, softmax_scale, *, kv_scale=None, out=None, wor
                                float(softmax_scale), b, s, h, d, rows, topk, _ptr(out),
                                _ptr(workspace), workspace.numel(), _stream(stream))
     _lib.check(st, "sa_sparse_attn")
+    return out
+
+
+def indexer_topk(score, start_pos, ratio, index_topk, offset, *, out=None, stream=None):
+    """The indexer's selection: score [b, s, n_comp] (f32 or bf16, n_comp = (start_pos + s) //
+    ratio) -> idx [b, s, k] int32, k = min(index_topk, n_comp): the top-k positions in position
+    order, + offset, -1 for a position the query does not see.  ``out`` may be a column slice of
+    a wider idx tensor (its row and batch strides are used)."""
+    if not isinstance(score, torch.Tensor) or not score.is_cuda or score.dim() != 3:
+        raise TypeError("score must be a 3-D CUDA tensor")
+    if score.dtype == torch.float32:
+        fmt = SA_SCORE_F32
+    elif score.dtype == torch.bfloat16:
+        fmt = SA_SCORE_BF16
+    else:
+        raise TypeError(f"score must be float32 or bfloat16, got {score.dtype}")
+    if not score.is_contiguous():
+        raise ValueError("score must be contiguous")
+    b, s, n = score.shape
+    k = min(int(index_topk), n)
+    if out is None:
+        out = torch.empty((b, s, k), dtype=torch.int32, device=score.device)
+    if out.dtype != torch.int32 or not out.is_cuda or tuple(out.shape) != (b, s, k) or (
+            k > 0 and out.stride(2) != 1):
+        raise ValueError(f"out must be a CUDA int32 tensor of shape {(b, s, k)} with unit column "
+                         "stride")
+    ld = out.stride(1) if s > 1 else max(k, out.stride(1))
+    bstride = out.stride(0) if b > 1 else s * ld
+    st = load().sa_indexer_topk(_ptr(score), fmt, b, s, n, int(start_pos), int(ratio),
+                                int(index_topk), int(offset), _ptr(out), ld, bstride,
+                                _stream(stream))
+    _lib.check(st, "sa_indexer_topk")
     return out
 
 

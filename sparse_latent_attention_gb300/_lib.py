@@ -8,6 +8,7 @@ library has not been built this module raises -- there is no fallback path.
 from __future__ import annotations
 
 import ctypes
+import glob
 import os
 import re
 import threading
@@ -19,6 +20,8 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "sparse_attn.h")
 (SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_INDEX, SA_ERR_WORKSPACE,
  SA_ERR_TIMEOUT) = range(7)
 SA_KV_BF16, SA_KV_FP8_E4M3 = 0, 1
+SA_SCORE_F32, SA_SCORE_BF16 = 0, 1
+SA_INDEXER_MAX_POSITIONS = 49152
 SA_STATUS_BYTES = 256
 
 _lock = threading.Lock()
@@ -50,6 +53,9 @@ def load() -> ctypes.CDLL:
         lib.sa_sparse_attn_rope.restype = i32
         lib.sa_sparse_attn_rope.argtypes = [P, P, P, i32, P, P, f32, i64, i64, i32, i32, i64, i32,
                                             P, P, sz, P, i64, i32, i64, P]
+        lib.sa_indexer_topk.restype = i32
+        lib.sa_indexer_topk.argtypes = [P, i32, i64, i64, i64, i64, i32, i32, ctypes.c_int32, P,
+                                        i64, i64, P]
         lib.sa_sparse_attn_workspace_size.restype = sz
         lib.sa_sparse_attn_workspace_size.argtypes = [i64, i64, i32, i32, i64, i32, i32]
         lib.sa_window_idxs.restype = i32
@@ -69,11 +75,13 @@ def load() -> ctypes.CDLL:
         return lib
 
 
-def declared_symbols(header: str = HEADER) -> list[str]:
-    """Names of the functions include/sparse_attn.h declares."""
-    text = open(header).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(sa_[a-z0-9_]+)\s*\(", text)))
+def declared_symbols() -> list[str]:
+    """Names of the functions the headers under include/ declare."""
+    names = set()
+    for header in sorted(glob.glob(os.path.join(os.path.dirname(HEADER), "*.h"))):
+        text = re.sub(r"/\*.*?\*/", "", open(header).read(), flags=re.S)
+        names.update(re.findall(r"\b(sa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def status_string(status: int) -> str:

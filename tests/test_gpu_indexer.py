@@ -1,0 +1,112 @@
+"""GPU parity of the indexer's selection (sa_indexer_topk) against the CPU oracle: bit-exact idx on
+the same seeded scores, ties included (both sides pick equal scores lowest position first)."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_latent_attention_gb300 as sa
+from sparse_latent_attention_gb300 import build
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    sa.load()
+    return torch.device("cuda:0")
+
+
+def _scores(rng, b, s, n, kind):
+    x = rng.standard_normal((b, s, n)).astype(np.float32)
+    if kind == "ties":        # eight levels: most picks are decided by the tie rule
+        x = np.round(x * 2.0).astype(np.float32)
+    elif kind == "specials":  # -0 / +0, -inf inside the visible range, whole rows equal
+        x[x > 1.2] = 0.0
+        x[x < -1.2] = -0.0
+        x[(x > 0.0) & (x < 0.1)] = -np.inf
+        x[:, ::7, :] = 0.5
+    return x
+
+
+def _run(dev, score_np, start_pos, ratio, topk, offset, bf16=False):
+    if bf16:
+        bits = (score_np.view(np.uint32) >> 16).astype(np.uint16)      # truncated to bf16
+        t = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        want = oracle.indexer_topk(bits, start_pos, ratio, topk, offset)
+    else:
+        t = torch.from_numpy(score_np).to(dev)
+        want = oracle.indexer_topk(score_np, start_pos, ratio, topk, offset)
+    got = sa.indexer_topk(t, start_pos, ratio, topk, offset)
+    torch.cuda.synchronize()
+    return got.cpu().numpy(), want
+
+
+CASES = [
+    # b, s, start_pos, ratio, index_topk, offset, kind, bf16
+    (1, 8192, 0, 4, 512, 8192, "normal", False),     # the compressed prefill: 2048 positions
+    (64, 1, 131071, 4, 2048, 128, "normal", False),  # long decode: 32768 positions
+    (1, 1000, 0, 4, 64, 128, "ties", True),          # bf16 scores, heavy ties
+    (2, 301, 0, 4, 48, 5, "specials", False),        # -0/+0, -inf, equal rows; ragged s
+    (1, 100, 0, 4, 512, 128, "normal", False),       # index_topk above the positions: k = 25
+    (3, 1, 40, 4, 1, 0, "ties", False),              # k = 1
+    (1, 257, 0, 1, 100, 0, "normal", False),         # ratio 1
+    (2, 1, 16383, 4, 700, 9, "ties", True),          # 4096 positions: 128-thread block
+    (2, 1, 16387, 4, 700, 9, "ties", True),          # 4097: 512-thread block
+    (2, 1, 65539, 4, 3000, 9, "normal", False),      # 16385: 1024-thread block
+    (2, 1, 4 * 49152 - 1, 4, 2048, 128, "ties", False),  # the largest row (192 KB of keys)
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"b{c[0]}s{c[1]}p{c[2]}r{c[3]}k{c[4]}{c[6]}"
+                         f"{'-bf16' if c[7] else ''}")
+def test_indexer_topk_bit_exact(dev, case):
+    b, s, start_pos, ratio, topk, offset, kind, bf16 = case
+    n = (start_pos + s) // ratio
+    rng = np.random.default_rng(b * 1000 + s + topk)
+    got, want = _run(dev, _scores(rng, b, s, n, kind), start_pos, ratio, topk, offset, bf16)
+    assert got.shape == want.shape
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} entries differ; first at {bad[:3].tolist()}"
+
+
+def test_indexer_topk_into_wider_idx(dev):
+    # the k columns written after the window columns of a wider idx tensor, nothing else touched
+    b, s, ratio, topk, W = 2, 1, 4, 300, 128
+    start_pos = 4 * 1000 - 1
+    n = (start_pos + s) // ratio
+    rng = np.random.default_rng(5)
+    sc = rng.standard_normal((b, s, n)).astype(np.float32)
+    idx = torch.full((b, s, W + topk + 3), -7, dtype=torch.int32, device=dev)
+    sa.indexer_topk(torch.from_numpy(sc).to(dev), start_pos, ratio, topk, W,
+                    out=idx[:, :, W:W + topk])
+    torch.cuda.synchronize()
+    got = idx.cpu().numpy()
+    assert (got[:, :, W:W + topk] == oracle.indexer_topk(sc, start_pos, ratio, topk, W)).all()
+    assert (got[:, :, :W] == -7).all() and (got[:, :, W + topk:] == -7).all()
+
+
+def test_indexer_topk_feeds_sparse_attn(dev):
+    # the selection's output is a valid idx for the attention call: window columns from
+    # window_idxs, compressed columns from indexer_topk, rows = window + compressed positions
+    b, s, h, d, ratio, W, topk = 1, 64, 64, 512, 4, 16, 8
+    n = s // ratio
+    rng = np.random.default_rng(6)
+    sc = torch.from_numpy(rng.standard_normal((b, s, n)).astype(np.float32)).to(dev)
+    idx = torch.empty((b, s, W + topk), dtype=torch.int32, device=dev)
+    sa.window_idxs(0, s, W, out=idx[:, :, :W])
+    sa.indexer_topk(sc, 0, ratio, topk, s, out=idx[:, :, W:])
+    q = torch.randn((b, s, h, d), device=dev).to(torch.bfloat16)
+    kv = torch.randn((b, s + n, d), device=dev).to(torch.bfloat16)
+    ws = sa.new_workspace(b, s, h, d, s + n, W + topk, device=dev)
+    sa.sparse_attn(q, kv, torch.zeros(h, device=dev), idx, d ** -0.5, workspace=ws)
+    torch.cuda.synchronize()
+    assert sa.read_status(ws) == 0  # every index inside [-1, rows)
+    comp = idx[:, :, W:].cpu().numpy()
+    assert ((comp == -1) | ((comp >= s) & (comp < s + n))).all()

@@ -21,7 +21,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == {"sa_sparse_attn", "sa_sparse_attn_workspace_size", "sa_window_idxs",
                           "sa_act_quant_fp8", "sa_read_status", "sa_status_string", "sa_version",
                           "sa_sparse_attn_static_scratch", "sa_window_write",
-                          "sa_sparse_attn_rope"}
+                          "sa_sparse_attn_rope", "sa_indexer_topk"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -108,6 +108,34 @@ def test_sparse_attn_rope_rejects_bad_arguments(lib, kw, code):
 def test_sparse_attn_rope_unsupported_on_forced_mma(lib, monkeypatch):
     monkeypatch.setenv("SA_FORCE_MMA", "1")
     assert _attn_rope(lib) == _lib.SA_ERR_UNSUPPORTED
+
+
+def _topk(lib, **kw):
+    a = dict(score=FAKE, fmt=0, b=2, s=1, n=32, start=127, ratio=4, topk=16, offset=128,
+             idx=FAKE2, ld=16, bstride=16, stream=None)
+    a.update(kw)
+    return lib.sa_indexer_topk(a["score"], a["fmt"], a["b"], a["s"], a["n"], a["start"], a["ratio"],
+                               a["topk"], a["offset"], a["idx"], a["ld"], a["bstride"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(fmt=2), _lib.SA_ERR_INVALID_ARG),
+    (dict(n=33), _lib.SA_ERR_INVALID_ARG),              # not (start_pos + s) // ratio
+    (dict(ratio=0), _lib.SA_ERR_INVALID_ARG),
+    (dict(offset=-1), _lib.SA_ERR_INVALID_ARG),
+    (dict(offset=(1 << 31) - 20), _lib.SA_ERR_INVALID_ARG),  # offset + n past int32
+    (dict(s=2, start=126), _lib.SA_ERR_UNSUPPORTED),    # chunked prefill
+    (dict(start=4 * 49153 - 1, n=49153), _lib.SA_ERR_UNSUPPORTED),  # past the shared-memory row
+    (dict(ld=15), _lib.SA_ERR_INVALID_ARG),             # rows shorter than k
+    (dict(bstride=15), _lib.SA_ERR_INVALID_ARG),        # sequences overlap
+    (dict(score=None), _lib.SA_ERR_INVALID_ARG),
+    (dict(idx=ctypes.c_void_p((1 << 41) + 2)), _lib.SA_ERR_INVALID_ARG),  # misaligned
+    (dict(idx=FAKE), _lib.SA_ERR_INVALID_ARG),          # idx overlaps score
+    (dict(topk=0, score=None), _lib.SA_OK),             # k == 0: nothing to write
+    (dict(b=0, score=None), _lib.SA_OK),
+])
+def test_indexer_topk_rejects_bad_arguments(lib, kw, code):
+    assert _topk(lib, **kw) == code
 
 
 def test_window_idxs_rejects_bad_arguments(lib):
