@@ -3,6 +3,7 @@ brute force and the pages' worked examples.  No GPU needed."""
 
 from __future__ import annotations
 
+import concurrent.futures
 import itertools
 import os
 
@@ -277,8 +278,9 @@ def test_e4m3_encode_saturates():
 def test_pow2_ceil_exhaustive():
     """Every positive normal f32 against 2 ** ceil(log2 v) from numpy's frexp."""
     lo, hi = 0x00800000, 0x7F7FFFFF
-    step = 1 << 24
-    for start in range(lo, hi + 1, step):
+    step = 1 << 22
+
+    def chunk(start):
         bits = np.arange(start, min(start + step, hi + 1), dtype=np.uint32)
         v = bits.view(np.float32)
         m, e = np.frexp(v)  # v = m * 2^e, 0.5 <= m < 1
@@ -286,7 +288,12 @@ def test_pow2_ceil_exhaustive():
         with np.errstate(over="ignore"):
             want = np.ldexp(np.float32(1.0), ce).astype(np.float32)
         got = oracle.pow2_ceil(v)
-        assert (got.view(np.uint32) == want.view(np.uint32)).all(), hex(start)
+        return start, bool((got.view(np.uint32) == want.view(np.uint32)).all())
+
+    # the chunks run on every core (numpy and the ctypes call release the GIL); still every value
+    with concurrent.futures.ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as pool:
+        for start, ok in pool.map(chunk, range(lo, hi + 1, step)):
+            assert ok, hex(start)
 
 
 # --------------------------------------------------------------------------------------------
