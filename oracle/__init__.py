@@ -69,6 +69,8 @@ def _load():
             lib.or_ring_write.argtypes = [P, P, i64, i64, i64, i64]
             lib.or_indexer_topk.restype = ctypes.c_int
             lib.or_indexer_topk.argtypes = [P, i64, i64, i64, i64, i64, i64, i64, P]
+            lib.or_candidate_blocks.restype = ctypes.c_int
+            lib.or_candidate_blocks.argtypes = [P, i64, i64, P, i64, i64, P]
             for name in ("or_bf16_round_array", "or_e4m3_encode_array", "or_e4m3_decode_array",
                          "or_pow2_ceil_array"):
                 getattr(lib, name).restype = None
@@ -161,14 +163,31 @@ def window_idxs(start_pos: int, seqlen: int, window: int) -> np.ndarray:
     return out
 
 
-def indexer_topk(score, start_pos: int, ratio: int, index_topk: int, offset: int) -> np.ndarray:
-    """The indexer's selection on score [b, s, n_comp] (f32, or bf16 bits as uint16, widened
-    exactly): idx [b, s, min(index_topk, n_comp)] int32 (see or_indexer_topk)."""
-    lib = _load()
+def _widen_scores(score) -> np.ndarray:
     score = np.asarray(score)
-    if score.dtype == np.uint16:
+    if score.dtype == np.uint16:  # bf16 bits, widened exactly
         score = (score.astype(np.uint32) << 16).view(np.float32)
-    sc = _c(score, np.float32)
+    return _c(score, np.float32)
+
+
+def visible_positions(s: int, n_comp: int, start_pos: int, ratio: int) -> np.ndarray:
+    """[s] positions each query of a call sees (Indexer.forward's compress_lens): (si + 1) //
+    ratio at a prefill, all n_comp at a decode step."""
+    if start_pos == 0:
+        return (np.arange(1, s + 1, dtype=np.int64) // ratio).astype(np.int64)
+    return np.full(s, n_comp, np.int64)
+
+
+def indexer_topk(score, start_pos: int, ratio: int, index_topk: int, offset: int,
+                 candidates=None) -> np.ndarray:
+    """The indexer's selection on score [b, s, n_comp] (f32, or bf16 bits as uint16, widened
+    exactly): idx [b, s, min(index_topk, n_comp)] int32 (see or_indexer_topk).  ``candidates``
+    (bool [b, s, n_comp]) first masks every score outside it to -inf, as a layer that uses
+    another layer's candidate blocks does (Indexer.forward, the uses_candidates branch)."""
+    lib = _load()
+    sc = _widen_scores(score)
+    if candidates is not None:
+        sc = np.where(np.asarray(candidates, bool), sc, np.float32(-np.inf)).astype(np.float32)
     b, s, n = sc.shape
     k = min(index_topk, n)
     out = np.empty((b, s, k), np.int32)
@@ -178,6 +197,33 @@ def indexer_topk(score, start_pos: int, ratio: int, index_topk: int, offset: int
     if rc != OK:
         raise ValueError(f"or_indexer_topk failed ({rc})")
     return out
+
+
+def candidate_blocks(logits, start_pos: int, ratio: int, topk_blocks: int,
+                     block_size: int) -> np.ndarray:
+    """select_candidate_blocks on logits [b, s, n_comp] (f32 or bf16 bits) of one indexer call at
+    start_pos: the bool mask [b, s, n_comp] of the positions in kept blocks (or_candidate_blocks),
+    each query seeing the positions visible_positions() gives it."""
+    sc = _widen_scores(logits)
+    b, s, n = sc.shape
+    vis = np.tile(visible_positions(s, n, start_pos, ratio), b)
+    return candidate_blocks_rows(sc.reshape(b * s, n), vis, topk_blocks, block_size).reshape(
+        b, s, n)
+
+
+def candidate_blocks_rows(logits, visible, topk_blocks: int, block_size: int) -> np.ndarray:
+    """or_candidate_blocks on rows [rows, width] (f32 or bf16 bits), row r seeing its first
+    visible[r] positions: bool mask [rows, width]."""
+    lib = _load()
+    sc = _widen_scores(logits)
+    rows, n = sc.shape
+    vis = np.ascontiguousarray(np.asarray(visible, np.int64))
+    out = np.empty((rows, n), np.uint8)
+    rc = lib.or_candidate_blocks(_ptr(sc), rows, n, _ptr(vis), topk_blocks, block_size,
+                                 _ptr(out))
+    if rc != OK:
+        raise ValueError(f"or_candidate_blocks failed ({rc})")
+    return out.astype(bool)
 
 
 def ring_write(ring: np.ndarray, rows: np.ndarray, start_pos: int) -> None:

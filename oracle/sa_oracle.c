@@ -14,6 +14,7 @@
  *          apply_rotary_emb (the inverse rotation of the output's rope dims).
  *   [IDX]  the same page, Indexer.forward: the selection that turns index scores into the
  *          compressed idx (visibility mask, top-k, position sort, -1 / offset).
+ *   [CAND] the same page, select_candidate_blocks: level one of the two-level top-k.
  *
  * Floating point: dot products, the softmax and the weighted sum are carried in f64; the only
  * rounding to a narrow type is the final bf16 round-to-nearest-even of o.  The act_quant steps
@@ -499,5 +500,57 @@ int or_indexer_topk(const float* score, int64_t b, int64_t s, int64_t n_comp, in
     }
     free(all);
     free(pick);
+    return 0;
+}
+
+/* [CAND] For every row r of logits [rows][width] whose query sees the first visible[r]
+ * positions (positions at or past visible[r] count as -inf, as the page's caller has already
+ * masked them):
+ *   block j's score = the highest logit among positions j*block_size .. (j+1)*block_size - 1
+ *                     (-inf past the row's end, the page's padding)
+ *   the block holding position visible[r] - 1 (the newest one the query sees) scores +inf;
+ *                     none when visible[r] == 0
+ *   the min(topk_blocks, blocks) highest-scoring blocks are picked (ties: lower block first);
+ *                     a pick whose score is -inf is dropped
+ *   mask[r][t] = 1 when t's block was kept, else 0.
+ * Returns 1 on a bad argument. */
+int or_candidate_blocks(const float* logits, int64_t rows, int64_t width, const int64_t* visible,
+                        int64_t topk_blocks, int64_t block_size, uint8_t* mask) {
+    if (rows < 0 || width < 0 || topk_blocks < 0 || block_size < 1) return 1;
+    if (rows == 0 || width == 0) return 0;
+    const int64_t nb = (width + block_size - 1) / block_size;
+    const int64_t k = topk_blocks < nb ? topk_blocks : nb;
+    scored_pos* blk = (scored_pos*)malloc((size_t)nb * sizeof *blk);
+    uint8_t* kept = (uint8_t*)malloc((size_t)nb);
+    if (!blk || !kept) {
+        free(blk);
+        free(kept);
+        return 1;
+    }
+    for (int64_t r = 0; r < rows; ++r) {
+        if (visible[r] < 0 || visible[r] > width) {
+            free(blk);
+            free(kept);
+            return 1;
+        }
+        const float* row = logits + r * width;
+        for (int64_t j = 0; j < nb; ++j) {
+            double best = -INFINITY;
+            for (int64_t t = j * block_size; t < (j + 1) * block_size && t < width; ++t) {
+                const double v = t < visible[r] ? (double)row[t] : -INFINITY;
+                if (v > best) best = v;
+            }
+            blk[j].v = best;
+            blk[j].pos = j;
+        }
+        if (visible[r] > 0) blk[(visible[r] - 1) / block_size].v = INFINITY;
+        qsort(blk, (size_t)nb, sizeof *blk, by_score_then_pos);
+        memset(kept, 0, (size_t)nb);
+        for (int64_t j = 0; j < k; ++j)
+            if (blk[j].v > -INFINITY) kept[blk[j].pos] = 1;
+        for (int64_t t = 0; t < width; ++t) mask[r * width + t] = kept[t / block_size];
+    }
+    free(blk);
+    free(kept);
     return 0;
 }

@@ -568,3 +568,83 @@ def test_indexer_topk_bf16_scores_and_bad_arguments():
         oracle.indexer_topk(x, 0, 4, 9, 0)                           # 50 != (0 + 1) // 4
     with pytest.raises(NotImplementedError):
         oracle.indexer_topk(np.zeros((1, 2, 50), np.float32), 99, 2, 9, 0)  # chunked prefill
+
+
+# --------------------------------------------------------------------------------------------
+# select_candidate_blocks ("DeepSeek V4.1" attention page)
+# --------------------------------------------------------------------------------------------
+
+def _golden_candidates():
+    g = {}
+    for line in open(os.path.join(GOLDEN, "candidate_blocks_example.txt")):
+        line = line.split("#")[0].strip()
+        if line:
+            k, _kind, *vals = line.split()
+            g[k] = [float(v) for v in vals]
+    return g
+
+
+def test_candidate_blocks_worked_example():
+    g = _golden_candidates()
+    row = np.array(g["logits"], np.float32)
+    bs = int(g["block_size"][0])
+    for key in ("v10_k2", "v5_k2", "v6_k1", "v0_k2", "v10_k5", "v3_k3"):
+        vis, k = (int(x) for x in key[1:].split("_k"))
+        got = oracle.candidate_blocks_rows(row[None], [vis], k, bs)[0]
+        assert got.astype(int).tolist() == [int(v) for v in g[key]], key
+
+
+def test_candidate_blocks_brute_force_with_ties():
+    # every subset of blocks on tiny rows with heavy ties and -inf: the kept blocks are the one
+    # subset of size min(k, blocks) that beats every block it leaves out (higher score, or equal
+    # at a lower block), the newest reachable block counting as +inf, minus its -inf members
+    rng = np.random.default_rng(95)
+    for _ in range(300):
+        width = int(rng.integers(1, 13))
+        bs = int(rng.integers(1, 5))
+        k = int(rng.integers(0, 6))
+        vis = int(rng.integers(0, width + 1))
+        row = rng.integers(-2, 3, size=width).astype(np.float32)
+        row[row == -2] = -np.inf
+        got = oracle.candidate_blocks_rows(row[None], [vis], k, bs)[0]
+        nb = -(-width // bs)
+        score = []
+        for j in range(nb):
+            vals = [row[t] if t < vis else -np.inf for t in range(j * bs, min((j + 1) * bs, width))]
+            score.append(max(vals))
+        if vis > 0:
+            score[(vis - 1) // bs] = np.inf
+        kk = min(k, nb)
+        picks = [S for S in itertools.combinations(range(nb), kk)
+                 if all(score[i] > score[j] or (score[i] == score[j] and i < j)
+                        for i in S for j in set(range(nb)) - set(S))]
+        assert len(picks) == 1
+        kept = {j for j in picks[0] if score[j] > -np.inf}
+        want = [t // bs in kept for t in range(width)]
+        assert got.tolist() == want, (row, vis, k, bs)
+
+
+def test_candidate_blocks_invariants_and_level_two():
+    rng = np.random.default_rng(96)
+    b, s, ratio, bs, kb = 2, 160, 4, 8, 3
+    n = s // ratio
+    x = rng.standard_normal((b, s, n)).astype(np.float32)
+    m = oracle.candidate_blocks(x, 0, ratio, kb, bs)
+    vis = oracle.visible_positions(s, n, 0, ratio)
+    for si in range(s):
+        blocks = m[:, si].reshape(b, -1, bs) if n % bs == 0 else None
+        assert blocks is not None and (blocks.all(-1) | ~blocks.any(-1)).all()  # whole blocks
+        nkept = blocks.any(-1).sum(-1)
+        assert (nkept == min(kb, -(-int(vis[si]) // bs))).all()              # reachable blocks
+        if vis[si] > 0:
+            assert m[:, si, vis[si] - 1].all()                                 # newest pinned
+    # level two: all-True candidates change nothing; the candidates bound every finite pick
+    full = np.ones_like(m)
+    assert (oracle.indexer_topk(x, 0, ratio, 16, 0, candidates=full) ==
+            oracle.indexer_topk(x, 0, ratio, 16, 0)).all()
+    two = oracle.indexer_topk(x, 0, ratio, 16, 0, candidates=m)
+    for bi in range(b):
+        for si in range(s):
+            picks = two[bi, si][two[bi, si] >= 0]
+            c = int(m[bi, si, :vis[si]].sum())  # visible candidate positions (finite scores)
+            assert int(m[bi, si, picks].sum()) == min(16, c)
