@@ -363,10 +363,12 @@ class GpuPath:
 
 
 COMPRESS_RATIO = 4  # the compressed workloads' ratio
+CANDIDATE_TOPK_BLOCKS, CANDIDATE_BLOCK_SIZE = 2048, 8  # the model config's candidate blocks
 
 
 def time_indexer_topk(wl, dev, steps, warmup, peaks):
-    """The indexer's selection (sa_indexer_topk) at this workload's compressed shape: index scores
+    """The indexer's two selection steps at this workload's compressed shape, each timed alone:
+    sa_indexer_topk and sa_candidate_blocks (2048 blocks of 8) on index scores
     [b, s, n_comp] f32 drawn N(0, 1), n_comp = (start_pos + s) / 4, -> the workload's compressed
     idx columns (index_topk = its non-window columns, offset = the rows before the compressed
     ones).  Timed alone like the step: L2 flushed, the call queued before its events."""
@@ -384,35 +386,47 @@ def time_indexer_topk(wl, dev, steps, warmup, peaks):
     out = torch.empty((wl.b, wl.s, k), dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def call():
-        sa.indexer_topk(score, wl.start_pos, COMPRESS_RATIO, index_topk, offset, out=out)
+    mask = torch.empty((wl.b, wl.s, n), dtype=torch.bool, device=dev)
 
-    for _ in range(warmup):
-        flush.zero_()
-        call()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    torch.cuda.synchronize()
-    for a, b in ev:
-        flush.zero_()
-        torch.cuda._sleep(HEAD_START_CYCLES)
-        a.record()
-        call()
-        b.record()
-    torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
-    # algorithmic bytes: the scores a query can see (a prefill's hidden positions are never read)
-    # and the idx written
+    def timed(call):
+        for _ in range(warmup):
+            flush.zero_()
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.zero_()
+            torch.cuda._sleep(HEAD_START_CYCLES)
+            a.record()
+            call()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+
+    def line(kernel, ms, alg, **extra):
+        gbs = alg / (ms * 1e-3) / 1e9
+        return {"kernel": kernel, "ms": round(ms, 4), "alg_bytes": int(alg), "bound": "hbm",
+                "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "queries": wl.b * wl.s,
+                "positions": n, **extra}
+
+    # algorithmic bytes: the scores a query can see (a prefill's hidden positions are never
+    # read), plus what is written (the idx, or one mask byte a position)
     if wl.start_pos == 0:
         seen = wl.b * sum((si + 1) // COMPRESS_RATIO for si in range(wl.s))
     else:
         seen = wl.b * wl.s * n
-    alg = 4 * seen + 4 * wl.b * wl.s * k
-    gbs = alg / (ms * 1e-3) / 1e9
-    return {"kernel": "indexer_topk_kernel", "ms": round(ms, 4), "alg_bytes": int(alg),
-            "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(gbs / peaks["hbm_gbs"], 4), "queries": wl.b * wl.s, "positions": n,
-            "k": k, "score": "f32"}
+    ms_topk = timed(lambda: sa.indexer_topk(score, wl.start_pos, COMPRESS_RATIO, index_topk,
+                                            offset, out=out))
+    ms_cand = timed(lambda: sa.candidate_blocks(score, wl.start_pos, COMPRESS_RATIO,
+                                                CANDIDATE_TOPK_BLOCKS, CANDIDATE_BLOCK_SIZE,
+                                                out=mask))
+    return {"indexer_topk": line("indexer_topk_kernel", ms_topk, 4 * seen + 4 * wl.b * wl.s * k,
+                                 k=k, score="f32"),
+            "candidate_blocks": line("candidate_blocks_kernel", ms_cand,
+                                     4 * seen + wl.b * wl.s * n, topk_blocks=CANDIDATE_TOPK_BLOCKS,
+                                     block_size=CANDIDATE_BLOCK_SIZE, score="f32")}
 
 
 def run_gpu(args, rank, world, local):
@@ -582,8 +596,7 @@ def run_gpu(args, rank, world, local):
         "library_source_hash": library_source_hash(),
     }
     if args.indexer_topk:
-        out["next_rows"] = {"indexer_topk": time_indexer_topk(wl, dev, args.steps, args.warmup,
-                                                              peaks)}
+        out["next_rows"] = time_indexer_topk(wl, dev, args.steps, args.warmup, peaks)
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     return out
@@ -745,7 +758,8 @@ def main(argv=None):
                     help="parts the end-to-end step's queries are copied and attended in "
                          "(0: one per 256 query tokens, at most 16)")
     ap.add_argument("--indexer-topk", action="store_true",
-                    help="also time the indexer's selection at the workload's compressed shape")
+                    help="also time the indexer's selection and candidate blocks at the "
+                         "workload's compressed shape")
     ap.add_argument("--rope", type=int, default=0, metavar="DIMS",
                     help="also rotate o's last DIMS dims back (inverse RoPE fused into the call; "
                          "the layer uses 64); 0 = off")

@@ -21,6 +21,7 @@ from ._lib import (SA_KV_BF16, SA_KV_FP8_E4M3, SA_SCORE_BF16, SA_SCORE_F32, SA_S
                    SparseAttnError, load, status_string)
 
 __all__ = ["sparse_attn", "window_idxs", "act_quant_fp8", "window_write", "indexer_topk",
+           "candidate_blocks",
            "workspace_size", "new_workspace", "read_status", "SparseAttnError", "SA_KV_BF16",
            "SA_KV_FP8_E4M3", "SA_SCORE_F32", "SA_SCORE_BF16", "load"]
 
@@ -114,22 +115,48 @@ def sparse_attn(q, kv, sink, idx, softmax_scale, *, kv_scale=None, out=None, wor
     return out
 
 
-def indexer_topk(score, start_pos, ratio, index_topk, offset, *, out=None, stream=None):
+def _score_format(score, name="score"):
+    if not isinstance(score, torch.Tensor) or not score.is_cuda or score.dim() != 3:
+        raise TypeError(f"{name} must be a 3-D CUDA tensor")
+    if not score.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if score.dtype == torch.float32:
+        return SA_SCORE_F32
+    if score.dtype == torch.bfloat16:
+        return SA_SCORE_BF16
+    raise TypeError(f"{name} must be float32 or bfloat16, got {score.dtype}")
+
+
+def candidate_blocks(logits, start_pos, ratio, topk_blocks, block_size, *, out=None,
+                     stream=None) -> torch.Tensor:
+    """select_candidate_blocks: logits [b, s, n_comp] (f32 or bf16) -> bool mask [b, s, n_comp],
+    True inside the topk_blocks best blocks of block_size positions (the block of the query's
+    newest visible position always kept, -inf blocks never)."""
+    fmt = _score_format(logits, "logits")
+    b, s, n = logits.shape
+    if out is None:
+        out = torch.empty((b, s, n), dtype=torch.bool, device=logits.device)
+    elif out.dtype != torch.bool or tuple(out.shape) != (b, s, n) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous bool tensor of shape {(b, s, n)}")
+    st = load().sa_candidate_blocks(_ptr(logits), fmt, b, s, n, int(start_pos), int(ratio),
+                                    int(topk_blocks), int(block_size), _ptr(out),
+                                    _stream(stream))
+    _lib.check(st, "sa_candidate_blocks")
+    return out
+
+
+def indexer_topk(score, start_pos, ratio, index_topk, offset, *, candidates=None, out=None,
+                 stream=None):
     """The indexer's selection: score [b, s, n_comp] (f32 or bf16, n_comp = (start_pos + s) //
     ratio) -> idx [b, s, k] int32, k = min(index_topk, n_comp): the top-k positions in position
-    order, + offset, -1 for a position the query does not see.  ``out`` may be a column slice of
-    a wider idx tensor (its row and batch strides are used)."""
-    if not isinstance(score, torch.Tensor) or not score.is_cuda or score.dim() != 3:
-        raise TypeError("score must be a 3-D CUDA tensor")
-    if score.dtype == torch.float32:
-        fmt = SA_SCORE_F32
-    elif score.dtype == torch.bfloat16:
-        fmt = SA_SCORE_BF16
-    else:
-        raise TypeError(f"score must be float32 or bfloat16, got {score.dtype}")
-    if not score.is_contiguous():
-        raise ValueError("score must be contiguous")
+    order, + offset, -1 for a position the query does not see.  ``candidates`` (bool [b, s,
+    n_comp], e.g. from candidate_blocks) masks the scores outside it first.  ``out`` may be a
+    column slice of a wider idx tensor (its row and batch strides are used)."""
+    fmt = _score_format(score)
     b, s, n = score.shape
+    if candidates is not None and (candidates.dtype != torch.bool or tuple(candidates.shape) !=
+                                   (b, s, n) or not candidates.is_contiguous()):
+        raise ValueError(f"candidates must be a contiguous bool tensor of shape {(b, s, n)}")
     k = min(int(index_topk), n)
     if out is None:
         out = torch.empty((b, s, k), dtype=torch.int32, device=score.device)
@@ -139,7 +166,8 @@ def indexer_topk(score, start_pos, ratio, index_topk, offset, *, out=None, strea
                          "stride")
     ld = out.stride(1) if s > 1 else max(k, out.stride(1))
     bstride = out.stride(0) if b > 1 else s * ld
-    st = load().sa_indexer_topk(_ptr(score), fmt, b, s, n, int(start_pos), int(ratio),
+    st = load().sa_indexer_topk(_ptr(score), fmt, _ptr(candidates), b, s, n, int(start_pos),
+                                int(ratio),
                                 int(index_topk), int(offset), _ptr(out), ld, bstride,
                                 _stream(stream))
     _lib.check(st, "sa_indexer_topk")

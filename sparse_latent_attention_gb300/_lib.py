@@ -54,8 +54,10 @@ def load() -> ctypes.CDLL:
         lib.sa_sparse_attn_rope.argtypes = [P, P, P, i32, P, P, f32, i64, i64, i32, i32, i64, i32,
                                             P, P, sz, P, i64, i32, i64, P]
         lib.sa_indexer_topk.restype = i32
-        lib.sa_indexer_topk.argtypes = [P, i32, i64, i64, i64, i64, i32, i32, ctypes.c_int32, P,
-                                        i64, i64, P]
+        lib.sa_indexer_topk.argtypes = [P, i32, P, i64, i64, i64, i64, i32, i32, ctypes.c_int32,
+                                        P, i64, i64, P]
+        lib.sa_candidate_blocks.restype = i32
+        lib.sa_candidate_blocks.argtypes = [P, i32, i64, i64, i64, i64, i32, i32, i32, P, P]
         lib.sa_sparse_attn_workspace_size.restype = sz
         lib.sa_sparse_attn_workspace_size.argtypes = [i64, i64, i32, i32, i64, i32, i32]
         lib.sa_window_idxs.restype = i32

@@ -110,3 +110,54 @@ def test_indexer_topk_feeds_sparse_attn(dev):
     assert sa.read_status(ws) == 0  # every index inside [-1, rows)
     comp = idx[:, :, W:].cpu().numpy()
     assert ((comp == -1) | ((comp >= s) & (comp < s + n))).all()
+
+
+CAND_CASES = [
+    # b, s, start_pos, ratio, topk_blocks, block_size, kind, bf16
+    (1, 8192, 0, 4, 2048, 8, "normal", False),      # the page's 2048 x 8 over a 2048-position prefill
+    (1, 8192, 0, 4, 64, 8, "normal", False),        # 64 of 256 blocks
+    (64, 1, 131071, 4, 2048, 8, "normal", False),   # long decode: 4096 blocks, half kept
+    (1, 1000, 0, 4, 16, 8, "ties", True),           # bf16, heavy ties between block maxima
+    (2, 301, 0, 4, 5, 7, "specials", False),        # -0/+0/-inf, equal rows, a ragged last block
+    (1, 64, 0, 4, 0, 8, "normal", False),           # no block wanted: all zeros
+    (2, 1, 4095, 4, 100, 1, "ties", False),         # every position its own block
+    (1, 40, 0, 1, 3, 64, "normal", False),          # one block, wider than the row
+]
+
+
+@pytest.mark.parametrize("case", CAND_CASES, ids=lambda c: f"b{c[0]}s{c[1]}p{c[2]}kb{c[4]}bs{c[5]}"
+                         f"{c[6]}{'-bf16' if c[7] else ''}")
+def test_candidate_blocks_bit_exact(dev, case):
+    b, s, start_pos, ratio, kb, bs, kind, bf16 = case
+    n = (start_pos + s) // ratio
+    rng = np.random.default_rng(b * 7 + s + kb + bs)
+    x = _scores(rng, b, s, n, kind)
+    if bf16:
+        bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+        t = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        want = oracle.candidate_blocks(bits, start_pos, ratio, kb, bs)
+    else:
+        t = torch.from_numpy(x).to(dev)
+        want = oracle.candidate_blocks(x, start_pos, ratio, kb, bs)
+    got = sa.candidate_blocks(t, start_pos, ratio, kb, bs)
+    torch.cuda.synchronize()
+    bad = np.argwhere(got.cpu().numpy() != want)
+    assert bad.size == 0, f"{len(bad)} mask bytes differ; first at {bad[:3].tolist()}"
+
+
+@pytest.mark.parametrize("b,s,start_pos,kb,topk", [(1, 2048, 0, 8, 64), (8, 1, 32767, 256, 512)])
+def test_two_level_selection_bit_exact(dev, b, s, start_pos, kb, topk):
+    # level one on one layer's scores, level two on another's inside the candidate blocks
+    ratio, bs, offset = 4, 8, 128
+    n = (start_pos + s) // ratio
+    rng = np.random.default_rng(kb + topk)
+    src = rng.standard_normal((b, s, n)).astype(np.float32)
+    own = rng.standard_normal((b, s, n)).astype(np.float32)
+    cand = sa.candidate_blocks(torch.from_numpy(src).to(dev), start_pos, ratio, kb, bs)
+    idx = sa.indexer_topk(torch.from_numpy(own).to(dev), start_pos, ratio, topk, offset,
+                          candidates=cand)
+    torch.cuda.synchronize()
+    cand_o = oracle.candidate_blocks(src, start_pos, ratio, kb, bs)
+    assert (cand.cpu().numpy() == cand_o).all()
+    want = oracle.indexer_topk(own, start_pos, ratio, topk, offset, candidates=cand_o)
+    assert (idx.cpu().numpy() == want).all()

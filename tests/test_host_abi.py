@@ -21,7 +21,8 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == {"sa_sparse_attn", "sa_sparse_attn_workspace_size", "sa_window_idxs",
                           "sa_act_quant_fp8", "sa_read_status", "sa_status_string", "sa_version",
                           "sa_sparse_attn_static_scratch", "sa_window_write",
-                          "sa_sparse_attn_rope", "sa_indexer_topk"}
+                          "sa_sparse_attn_rope", "sa_indexer_topk",
+                          "sa_candidate_blocks"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -111,11 +112,12 @@ def test_sparse_attn_rope_unsupported_on_forced_mma(lib, monkeypatch):
 
 
 def _topk(lib, **kw):
-    a = dict(score=FAKE, fmt=0, b=2, s=1, n=32, start=127, ratio=4, topk=16, offset=128,
-             idx=FAKE2, ld=16, bstride=16, stream=None)
+    a = dict(score=FAKE, fmt=0, cand=None, b=2, s=1, n=32, start=127, ratio=4, topk=16,
+             offset=128, idx=FAKE2, ld=16, bstride=16, stream=None)
     a.update(kw)
-    return lib.sa_indexer_topk(a["score"], a["fmt"], a["b"], a["s"], a["n"], a["start"], a["ratio"],
-                               a["topk"], a["offset"], a["idx"], a["ld"], a["bstride"], a["stream"])
+    return lib.sa_indexer_topk(a["score"], a["fmt"], a["cand"], a["b"], a["s"], a["n"], a["start"],
+                               a["ratio"], a["topk"], a["offset"], a["idx"], a["ld"], a["bstride"],
+                               a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -133,9 +135,34 @@ def _topk(lib, **kw):
     (dict(idx=FAKE), _lib.SA_ERR_INVALID_ARG),          # idx overlaps score
     (dict(topk=0, score=None), _lib.SA_OK),             # k == 0: nothing to write
     (dict(b=0, score=None), _lib.SA_OK),
+    (dict(cand=ctypes.c_void_p((1 << 41) + 8)), _lib.SA_ERR_INVALID_ARG),  # candidates overlap idx
 ])
 def test_indexer_topk_rejects_bad_arguments(lib, kw, code):
     assert _topk(lib, **kw) == code
+
+
+def _cand(lib, **kw):
+    a = dict(logits=FAKE, fmt=0, b=2, s=1, n=32, start=127, ratio=4, kb=2, bs=8, mask=FAKE2,
+             stream=None)
+    a.update(kw)
+    return lib.sa_candidate_blocks(a["logits"], a["fmt"], a["b"], a["s"], a["n"], a["start"],
+                                   a["ratio"], a["kb"], a["bs"], a["mask"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(fmt=5), _lib.SA_ERR_INVALID_ARG),
+    (dict(n=31), _lib.SA_ERR_INVALID_ARG),              # not (start_pos + s) // ratio
+    (dict(bs=0), _lib.SA_ERR_INVALID_ARG),
+    (dict(kb=-1), _lib.SA_ERR_INVALID_ARG),
+    (dict(s=2, start=126), _lib.SA_ERR_UNSUPPORTED),    # chunked prefill
+    (dict(start=4 * 49153 - 1, n=49153, bs=1), _lib.SA_ERR_UNSUPPORTED),  # too many blocks
+    (dict(mask=None), _lib.SA_ERR_INVALID_ARG),
+    (dict(logits=None), _lib.SA_ERR_INVALID_ARG),
+    (dict(mask=ctypes.c_void_p((1 << 40) + 64)), _lib.SA_ERR_INVALID_ARG),  # inside the logits
+    (dict(b=0, logits=None, mask=None), _lib.SA_OK),
+])
+def test_candidate_blocks_rejects_bad_arguments(lib, kw, code):
+    assert _cand(lib, **kw) == code
 
 
 def test_window_idxs_rejects_bad_arguments(lib):
