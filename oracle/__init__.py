@@ -71,6 +71,8 @@ def _load():
             lib.or_indexer_topk.argtypes = [P, i64, i64, i64, i64, i64, i64, i64, P]
             lib.or_candidate_blocks.restype = ctypes.c_int
             lib.or_candidate_blocks.argtypes = [P, i64, i64, P, i64, i64, P]
+            lib.or_hc_split_sinkhorn.restype = ctypes.c_int
+            lib.or_hc_split_sinkhorn.argtypes = [P, i64, i64, P, P, i64, ctypes.c_double, P, P, P]
             for name in ("or_bf16_round_array", "or_e4m3_encode_array", "or_e4m3_decode_array",
                          "or_pow2_ceil_array"):
                 getattr(lib, name).restype = None
@@ -224,6 +226,28 @@ def candidate_blocks_rows(logits, visible, topk_blocks: int, block_size: int) ->
     if rc != OK:
         raise ValueError(f"or_candidate_blocks failed ({rc})")
     return out.astype(bool)
+
+
+def hc_split_sinkhorn(mixes, hc_scale, hc_base, hc: int = 4, iters: int = 20,
+                      eps: float = 1e-6):
+    """hc_split_sinkhorn on mixes [..., (2 + hc) * hc] f32 with hc_scale [3], hc_base
+    [(2 + hc) * hc] (f32): (pre [..., hc], post [..., hc], comb [..., hc, hc]) in f64."""
+    lib = _load()
+    m = _c(mixes, np.float32)
+    lead = m.shape[:-1]
+    mix = (2 + hc) * hc
+    if m.shape[-1] != mix:
+        raise ValueError(f"mixes rows must have {mix} values")
+    n = int(np.prod(lead)) if lead else 1
+    sc, bs = _c(hc_scale, np.float32), _c(hc_base, np.float32)
+    pre = np.empty((n, hc), np.float64)
+    post = np.empty((n, hc), np.float64)
+    comb = np.empty((n, hc, hc), np.float64)
+    rc = lib.or_hc_split_sinkhorn(_ptr(m), n, hc, _ptr(sc), _ptr(bs), iters, eps, _ptr(pre),
+                                  _ptr(post), _ptr(comb))
+    if rc != OK:
+        raise ValueError(f"or_hc_split_sinkhorn failed ({rc})")
+    return pre.reshape(lead + (hc,)), post.reshape(lead + (hc,)), comb.reshape(lead + (hc, hc))
 
 
 def ring_write(ring: np.ndarray, rows: np.ndarray, start_pos: int) -> None:

@@ -15,6 +15,8 @@
  *   [IDX]  the same page, Indexer.forward: the selection that turns index scores into the
  *          compressed idx (visibility mask, top-k, position sort, -1 / offset).
  *   [CAND] the same page, select_candidate_blocks: level one of the two-level top-k.
+ *   [HC]   the same page, hc_split_sinkhorn (and its kernel): a Hyper-Connections block's mixes
+ *          split into pre / post weights and a Sinkhorn-normalised comb matrix.
  *
  * Floating point: dot products, the softmax and the weighted sum are carried in f64; the only
  * rounding to a narrow type is the final bf16 round-to-nearest-even of o.  The act_quant steps
@@ -552,5 +554,65 @@ int or_candidate_blocks(const float* logits, int64_t rows, int64_t width, const 
     }
     free(blk);
     free(kept);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* [HC] hc_split_sinkhorn                                                                     */
+/* ------------------------------------------------------------------------------------------ */
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* [HC] For every token i of mixes [n][(2 + hc) * hc], with scale [3] and base [(2 + hc) * hc]
+ * (a_j = mixes[i][j] * scale[.] + base[j]):
+ *   pre[i][j]  = sigmoid(a_j) + eps,  using scale[0], j < hc
+ *   post[i][j] = 2 sigmoid(a_{hc + j}),  scale[1]
+ *   comb[i]    = the hc x hc matrix a_{2 hc + j hc + k} (row j, column k),  scale[2];
+ *                each row replaced by its softmax, plus eps;
+ *                each column divided by (its sum + eps);
+ *                then iters - 1 times: each row divided by (its sum + eps), then each column.
+ * In f64 from the f32 inputs (the page works in f32).  Returns 1 on a bad argument. */
+int or_hc_split_sinkhorn(const float* mixes, int64_t n, int64_t hc, const float* scale,
+                         const float* base, int64_t iters, double eps, double* pre, double* post,
+                         double* comb) {
+    if (n < 0 || hc < 1 || hc > 16 || iters < 1) return 1;
+    const int64_t mix = (2 + hc) * hc;
+    double c[16][16];
+    for (int64_t i = 0; i < n; ++i) {
+        const float* m = mixes + i * mix;
+        for (int64_t j = 0; j < hc; ++j) {
+            pre[i * hc + j] = sigmoid((double)m[j] * scale[0] + base[j]) + eps;
+            post[i * hc + j] = 2.0 * sigmoid((double)m[hc + j] * scale[1] + base[hc + j]);
+        }
+        for (int64_t j = 0; j < hc; ++j)
+            for (int64_t k = 0; k < hc; ++k)
+                c[j][k] = (double)m[2 * hc + j * hc + k] * scale[2] + base[2 * hc + j * hc + k];
+        /* softmax along each row, plus eps */
+        for (int64_t j = 0; j < hc; ++j) {
+            double mx = c[j][0], sum = 0.0;
+            for (int64_t k = 1; k < hc; ++k) mx = c[j][k] > mx ? c[j][k] : mx;
+            for (int64_t k = 0; k < hc; ++k) {
+                c[j][k] = exp(c[j][k] - mx);
+                sum += c[j][k];
+            }
+            for (int64_t k = 0; k < hc; ++k) c[j][k] = c[j][k] / sum + eps;
+        }
+        for (int64_t it = 0; it < iters; ++it) {
+            if (it > 0) { /* rows (the first round's row step is the softmax) */
+                for (int64_t j = 0; j < hc; ++j) {
+                    double sum = 0.0;
+                    for (int64_t k = 0; k < hc; ++k) sum += c[j][k];
+                    for (int64_t k = 0; k < hc; ++k) c[j][k] /= sum + eps;
+                }
+            }
+            for (int64_t k = 0; k < hc; ++k) { /* columns */
+                double sum = 0.0;
+                for (int64_t j = 0; j < hc; ++j) sum += c[j][k];
+                for (int64_t j = 0; j < hc; ++j) c[j][k] /= sum + eps;
+            }
+        }
+        for (int64_t j = 0; j < hc; ++j)
+            for (int64_t k = 0; k < hc; ++k) comb[(i * hc + j) * hc + k] = c[j][k];
+    }
     return 0;
 }

@@ -648,3 +648,79 @@ def test_candidate_blocks_invariants_and_level_two():
             picks = two[bi, si][two[bi, si] >= 0]
             c = int(m[bi, si, :vis[si]].sum())  # visible candidate positions (finite scores)
             assert int(m[bi, si, picks].sum()) == min(16, c)
+
+
+# --------------------------------------------------------------------------------------------
+# hc_split_sinkhorn ("DeepSeek V4.1" attention page)
+# --------------------------------------------------------------------------------------------
+
+def _hc_case(seed, n=64, hc=4, spread=1.0):
+    rng = np.random.default_rng(seed)
+    mix = (2 + hc) * hc
+    m = (rng.standard_normal((n, mix)) * spread).astype(np.float32)
+    sc = rng.uniform(0.5, 2.0, 3).astype(np.float32)
+    base = (rng.standard_normal(mix) * 0.5).astype(np.float32)
+    return m, sc, base
+
+
+def test_hc_pre_post_are_library_sigmoids():
+    m, sc, base = _hc_case(101)
+    pre, post, _ = oracle.hc_split_sinkhorn(m, sc, base, 4, 20, 1e-6)
+    a = m.astype(np.float64)
+    want_pre = scipy.special.expit(a[:, :4] * np.float64(sc[0]) + base[:4]) + 1e-6
+    want_post = 2.0 * scipy.special.expit(a[:, 4:8] * np.float64(sc[1]) + base[4:8])
+    assert np.allclose(pre, want_pre, rtol=0, atol=1e-15)
+    assert np.allclose(post, want_post, rtol=0, atol=1e-15)
+
+
+def test_hc_one_round_is_softmax_then_column_normalisation():
+    # iters = 1: the row softmax (scipy) plus eps, then each column over (its sum + eps)
+    m, sc, base = _hc_case(102, hc=3)
+    eps = 1e-3
+    _, _, comb = oracle.hc_split_sinkhorn(m, sc, base, 3, 1, eps)
+    logits = (m[:, 6:].astype(np.float64) * np.float64(sc[2]) + base[6:]).reshape(-1, 3, 3)
+    x = scipy.special.softmax(logits, axis=-1) + eps
+    want = x / (x.sum(axis=-2, keepdims=True) + eps)
+    assert np.allclose(comb, want, rtol=1e-13, atol=0)
+    assert not np.allclose(comb, np.swapaxes(want, -1, -2), atol=1e-3)  # rows and columns differ
+
+
+def test_hc_uniform_logits_follow_the_scalar_recurrence():
+    # equal logits keep every entry equal: x0 = 1/hc + eps, then x <- x / (hc x + eps) once per
+    # normalisation (one column step, then a row and a column step per extra round)
+    hc, iters, eps = 4, 20, 1e-2
+    m = np.zeros((2, 24), np.float32)
+    _, _, comb = oracle.hc_split_sinkhorn(m, np.ones(3, np.float32), np.zeros(24, np.float32),
+                                          hc, iters, eps)
+    x = 1.0 / hc + eps
+    for _ in range(2 * iters - 1):
+        x = x / (hc * x + eps)
+    assert np.allclose(comb, x, rtol=1e-14, atol=0)
+
+
+def test_hc_sinkhorn_limit_is_doubly_stochastic():
+    m, sc, base = _hc_case(103, n=200, spread=2.0)
+    _, _, comb = oracle.hc_split_sinkhorn(m, sc, base, 4, 20, 1e-6)
+    cols = comb.sum(axis=-2)
+    rows = comb.sum(axis=-1)
+    assert np.abs(cols - 1).max() < 1e-5           # the last step normalises the columns
+    assert np.abs(rows - 1).max() < 5e-3           # 20 rounds: the rows are close ...
+    # ... and more rounds move them to the fixed point, where only eps keeps the sums below 1
+    _, _, c40 = oracle.hc_split_sinkhorn(m, sc, base, 4, 40, 1e-6)
+    _, _, c100 = oracle.hc_split_sinkhorn(m, sc, base, 4, 100, 1e-6)
+    assert np.abs(c40.sum(-1) - 1).max() < np.abs(rows - 1).max()
+    assert np.abs(c100.sum(-1) - 1).max() < 2e-6 and np.abs(c100.sum(-2) - 1).max() < 2e-6
+
+
+def test_hc_comb_is_permutation_equivariant():
+    # permuting the logits' rows by P and columns by Q permutes comb the same way
+    m, sc, base = _hc_case(104, n=16)
+    rng = np.random.default_rng(5)
+    P, Q = rng.permutation(4), rng.permutation(4)
+    sc[2], base[8:] = 1.0, 0.0  # a shared affine map keeps the permutation exact
+    logit = m[:, 8:].reshape(-1, 4, 4)
+    m2 = m.copy()
+    m2[:, 8:] = logit[:, P][:, :, Q].reshape(-1, 16)
+    _, _, c1 = oracle.hc_split_sinkhorn(m, sc, base)
+    _, _, c2 = oracle.hc_split_sinkhorn(m2, sc, base)
+    assert np.allclose(c2, c1[:, P][:, :, Q], rtol=1e-12, atol=0)
