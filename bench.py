@@ -429,6 +429,40 @@ def time_indexer_topk(wl, dev, steps, warmup, peaks):
                                      block_size=CANDIDATE_BLOCK_SIZE, score="f32")}
 
 
+HC_TOKENS = 1 << 20  # token rows of the hc_split_sinkhorn timing (201 MB in + out, past L2)
+
+
+def time_hc_split_sinkhorn(dev, steps, warmup, peaks):
+    """hc_split_sinkhorn (hc 4, 20 rounds, eps 1e-6) on 2^20 token rows of N(0, 1) mixes, timed
+    alone like the step; algorithmic bytes = the mixes read and pre / post / comb written."""
+    import torch
+
+    import sparse_latent_attention_gb300 as sa
+    g = torch.Generator(device=dev).manual_seed(12)
+    mixes = torch.randn((HC_TOKENS, 24), generator=g, device=dev)
+    scale = torch.ones(3, device=dev)
+    base = torch.zeros(24, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        sa.hc_split_sinkhorn(mixes, scale, base)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)
+        a.record()
+        sa.hc_split_sinkhorn(mixes, scale, base)
+        b.record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    alg = HC_TOKENS * (24 + 24) * 4
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"kernel": "hc_split_sinkhorn_kernel", "ms": round(ms, 4), "alg_bytes": int(alg),
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "tokens": HC_TOKENS, "hc": 4, "iters": 20}
+
+
 def run_gpu(args, rank, world, local):
     import torch
     torch.cuda.set_device(local)
@@ -597,6 +631,11 @@ def run_gpu(args, rank, world, local):
     }
     if args.indexer_topk:
         out["next_rows"] = time_indexer_topk(wl, dev, args.steps, args.warmup, peaks)
+    if args.hc_sinkhorn:
+        out.setdefault("next_rows", {})
+        out["next_rows"] = dict(out["next_rows"] or {},
+                                hc_split_sinkhorn=time_hc_split_sinkhorn(dev, args.steps,
+                                                                         args.warmup, peaks))
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     return out
@@ -760,6 +799,8 @@ def main(argv=None):
     ap.add_argument("--indexer-topk", action="store_true",
                     help="also time the indexer's selection and candidate blocks at the "
                          "workload's compressed shape")
+    ap.add_argument("--hc-sinkhorn", action="store_true",
+                    help="also time hc_split_sinkhorn on 2^20 token rows")
     ap.add_argument("--rope", type=int, default=0, metavar="DIMS",
                     help="also rotate o's last DIMS dims back (inverse RoPE fused into the call; "
                          "the layer uses 64); 0 = off")

@@ -21,7 +21,7 @@ from ._lib import (SA_KV_BF16, SA_KV_FP8_E4M3, SA_SCORE_BF16, SA_SCORE_F32, SA_S
                    SparseAttnError, load, status_string)
 
 __all__ = ["sparse_attn", "window_idxs", "act_quant_fp8", "window_write", "indexer_topk",
-           "candidate_blocks",
+           "candidate_blocks", "hc_split_sinkhorn",
            "workspace_size", "new_workspace", "read_status", "SparseAttnError", "SA_KV_BF16",
            "SA_KV_FP8_E4M3", "SA_SCORE_F32", "SA_SCORE_BF16", "load"]
 
@@ -125,6 +125,28 @@ def _score_format(score, name="score"):
     if score.dtype == torch.bfloat16:
         return SA_SCORE_BF16
     raise TypeError(f"{name} must be float32 or bfloat16, got {score.dtype}")
+
+
+def hc_split_sinkhorn(mixes, hc_scale, hc_base, hc=4, sinkhorn_iters=20, eps=1e-6, *,
+                      stream=None):
+    """hc_split_sinkhorn: mixes [..., (2 + hc) * hc] f32, hc_scale [3], hc_base [(2 + hc) * hc]
+    -> (pre [..., hc], post [..., hc], comb [..., hc, hc]), all f32."""
+    for t, name in ((mixes, "mixes"), (hc_scale, "hc_scale"), (hc_base, "hc_base")):
+        _need(t, name, torch.float32, mixes.device)
+    mix = (2 + hc) * hc
+    if mixes.shape[-1] != mix or tuple(hc_scale.shape) != (3,) or tuple(hc_base.shape) != (mix,):
+        raise ValueError(f"shapes do not fit hc = {hc}: mixes [..., {mix}], hc_scale [3], "
+                         f"hc_base [{mix}]")
+    lead = tuple(mixes.shape[:-1])
+    n = mixes.numel() // mix
+    pre = torch.empty(lead + (hc,), dtype=torch.float32, device=mixes.device)
+    post = torch.empty_like(pre)
+    comb = torch.empty(lead + (hc, hc), dtype=torch.float32, device=mixes.device)
+    st = load().sa_hc_split_sinkhorn(_ptr(mixes), n, hc, _ptr(hc_scale), _ptr(hc_base),
+                                     int(sinkhorn_iters), float(eps), _ptr(pre), _ptr(post),
+                                     _ptr(comb), _stream(stream))
+    _lib.check(st, "sa_hc_split_sinkhorn")
+    return pre, post, comb
 
 
 def candidate_blocks(logits, start_pos, ratio, topk_blocks, block_size, *, out=None,

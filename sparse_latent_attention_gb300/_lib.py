@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
         lib.sa_indexer_topk.restype = i32
         lib.sa_indexer_topk.argtypes = [P, i32, P, i64, i64, i64, i64, i32, i32, ctypes.c_int32,
                                         P, i64, i64, P]
+        lib.sa_hc_split_sinkhorn.restype = i32
+        lib.sa_hc_split_sinkhorn.argtypes = [P, i64, i32, P, P, i32, f32, P, P, P, P]
         lib.sa_candidate_blocks.restype = i32
         lib.sa_candidate_blocks.argtypes = [P, i32, i64, i64, i64, i64, i32, i32, i32, P, P]
         lib.sa_sparse_attn_workspace_size.restype = sz

@@ -1,0 +1,154 @@
+// hc_split_sinkhorn ("DeepSeek V4.1" attention page): a Hyper-Connections block's per-token mixes
+// split into pre / post weights and a Sinkhorn-normalised comb matrix, and its C ABI entry
+// (include/sa_hc.h).
+//
+// One thread per token.  A block's 256 rows of mixes are staged through shared memory (a
+// coalesced copy in, one padded row per thread), computed in registers in f32, and the outputs
+// leave through the same buffer as coalesced stores.  Memory-bound: 96 bytes in and 96 out per
+// token at hc = 4.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sa_hc.h"
+
+namespace {
+
+constexpr int kTok = 256;  // tokens (threads) per block
+
+template <int HC>
+__global__ void __launch_bounds__(kTok)
+    hc_split_sinkhorn_kernel(const float* __restrict__ mixes, int64_t n,
+                             const float* __restrict__ scale, const float* __restrict__ base,
+                             int iters, float eps, float* __restrict__ pre,
+                             float* __restrict__ post, float* __restrict__ comb) {
+    constexpr int kMix = (2 + HC) * HC;  // values a token has, in and out
+    constexpr int kStride = kMix + 1;    // odd row stride: a thread's row reads are conflict-free
+    __shared__ float rows[kTok * kStride];
+    __shared__ float sb[kMix];
+    __shared__ float ss[3];
+    const int tid = threadIdx.x;
+    const int64_t t0 = (int64_t)blockIdx.x * kTok;
+    const int ntok = (int)min((int64_t)kTok, n - t0);
+    const float* src = mixes + t0 * kMix;
+    for (int e = tid; e < ntok * kMix; e += kTok) {
+        const int r = e / kMix;
+        rows[r * kStride + (e - r * kMix)] = __ldg(src + e);
+    }
+    if (tid < kMix) sb[tid] = __ldg(base + tid);
+    if (tid < 3) ss[tid] = __ldg(scale + tid);
+    __syncthreads();
+
+    float pr[HC], po[HC], c[HC][HC];
+    if (tid < ntok) {
+        const float* m = rows + tid * kStride;
+#pragma unroll
+        for (int j = 0; j < HC; ++j) {
+            pr[j] = 1.f / (1.f + expf(-(m[j] * ss[0] + sb[j]))) + eps;
+            po[j] = 2.f / (1.f + expf(-(m[HC + j] * ss[1] + sb[HC + j])));
+        }
+#pragma unroll
+        for (int j = 0; j < HC; ++j)
+#pragma unroll
+            for (int k = 0; k < HC; ++k)
+                c[j][k] = m[2 * HC + j * HC + k] * ss[2] + sb[2 * HC + j * HC + k];
+        // each row: softmax, plus eps
+#pragma unroll
+        for (int j = 0; j < HC; ++j) {
+            float mx = c[j][0];
+#pragma unroll
+            for (int k = 1; k < HC; ++k) mx = fmaxf(mx, c[j][k]);
+            float sum = 0.f;
+#pragma unroll
+            for (int k = 0; k < HC; ++k) {
+                c[j][k] = expf(c[j][k] - mx);
+                sum += c[j][k];
+            }
+#pragma unroll
+            for (int k = 0; k < HC; ++k) c[j][k] = c[j][k] / sum + eps;
+        }
+        // a column step, then iters - 1 rounds of a row step and a column step
+#pragma unroll 1
+        for (int it = 0; it < iters; ++it) {
+            if (it > 0) {
+#pragma unroll
+                for (int j = 0; j < HC; ++j) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int k = 0; k < HC; ++k) sum += c[j][k];
+                    const float d = sum + eps;
+#pragma unroll
+                    for (int k = 0; k < HC; ++k) c[j][k] = c[j][k] / d;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < HC; ++k) {
+                float sum = 0.f;
+#pragma unroll
+                for (int j = 0; j < HC; ++j) sum += c[j][k];
+                const float d = sum + eps;
+#pragma unroll
+                for (int j = 0; j < HC; ++j) c[j][k] = c[j][k] / d;
+            }
+        }
+    }
+    __syncthreads();  // every row has been read: the buffer now takes the outputs
+    if (tid < ntok) {
+        float* o = rows + tid * kStride;
+#pragma unroll
+        for (int j = 0; j < HC; ++j) {
+            o[j] = pr[j];
+            o[HC + j] = po[j];
+#pragma unroll
+            for (int k = 0; k < HC; ++k) o[2 * HC + j * HC + k] = c[j][k];
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < ntok * HC; e += kTok) {
+        const int r = e / HC, j = e - r * HC;
+        pre[t0 * HC + e] = rows[r * kStride + j];
+        post[t0 * HC + e] = rows[r * kStride + HC + j];
+    }
+    for (int e = tid; e < ntok * HC * HC; e += kTok) {
+        const int r = e / (HC * HC);
+        comb[t0 * HC * HC + e] = rows[r * kStride + 2 * HC + (e - r * HC * HC)];
+    }
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+}  // namespace
+
+extern "C" sa_status sa_hc_split_sinkhorn(const float* mixes, int64_t n, int hc,
+                                          const float* hc_scale, const float* hc_base,
+                                          int sinkhorn_iters, float eps, float* pre, float* post,
+                                          float* comb, void* stream) {
+    if (n < 0 || hc < 1 || sinkhorn_iters < 1) return SA_ERR_INVALID_ARG;
+    if (hc != 4) return SA_ERR_UNSUPPORTED;
+    if (n > (int64_t)INT32_MAX * kTok) return SA_ERR_INVALID_ARG;  // one block per 256 tokens
+    if (n == 0) return SA_OK;
+    if (!mixes || !hc_scale || !hc_base || !pre || !post || !comb) return SA_ERR_INVALID_ARG;
+    if (!aligned(mixes, 16) || !aligned(hc_scale, 4) || !aligned(hc_base, 4) ||
+        !aligned(pre, 4) || !aligned(post, 4) || !aligned(comb, 4))
+        return SA_ERR_INVALID_ARG;
+    const size_t mix = (size_t)(2 + hc) * hc;
+    const size_t in_b = (size_t)n * mix * 4, pp_b = (size_t)n * hc * 4, c_b = (size_t)n * hc * hc * 4;
+    const void* outs[3] = {pre, post, comb};
+    const size_t out_b[3] = {pp_b, pp_b, c_b};
+    for (int i = 0; i < 3; ++i) {
+        if (overlaps(outs[i], out_b[i], mixes, in_b) || overlaps(outs[i], out_b[i], hc_scale, 12) ||
+            overlaps(outs[i], out_b[i], hc_base, mix * 4))
+            return SA_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], out_b[i], outs[j], out_b[j])) return SA_ERR_INVALID_ARG;
+    }
+    const int64_t blocks = (n + kTok - 1) / kTok;
+    hc_split_sinkhorn_kernel<4><<<(unsigned)blocks, kTok, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        mixes, n, hc_scale, hc_base, sinkhorn_iters, eps, pre, post, comb);
+    return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}

@@ -22,7 +22,7 @@ def test_exports_every_declared_symbol(lib):
                           "sa_act_quant_fp8", "sa_read_status", "sa_status_string", "sa_version",
                           "sa_sparse_attn_static_scratch", "sa_window_write",
                           "sa_sparse_attn_rope", "sa_indexer_topk",
-                          "sa_candidate_blocks"}
+                          "sa_candidate_blocks", "sa_hc_split_sinkhorn"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -207,3 +207,29 @@ def test_window_write_rejects_bad_arguments(lib):
 
 def test_read_status_rejects_null(lib):
     assert lib.sa_read_status(None, 0, None) == _lib.SA_ERR_INVALID_ARG
+
+
+def _hc(lib, **kw):
+    a = dict(mixes=FAKE, n=100, hc=4, scale=ctypes.c_void_p((1 << 40) + (1 << 20)),
+             base=ctypes.c_void_p((1 << 40) + (1 << 21)), iters=20, eps=1e-6,
+             pre=ctypes.c_void_p(1 << 41), post=ctypes.c_void_p((1 << 41) + (1 << 20)),
+             comb=ctypes.c_void_p((1 << 41) + (1 << 21)), stream=None)
+    a.update(kw)
+    return lib.sa_hc_split_sinkhorn(a["mixes"], a["n"], a["hc"], a["scale"], a["base"], a["iters"],
+                                    a["eps"], a["pre"], a["post"], a["comb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(hc=3), _lib.SA_ERR_UNSUPPORTED),              # only the model's hc_mult = 4
+    (dict(iters=0), _lib.SA_ERR_INVALID_ARG),
+    (dict(n=-1), _lib.SA_ERR_INVALID_ARG),
+    (dict(n=(2**31 - 1) * 256 + 1), _lib.SA_ERR_INVALID_ARG),  # past the grid
+    (dict(mixes=ctypes.c_void_p((1 << 40) + 4)), _lib.SA_ERR_INVALID_ARG),  # not 16-byte aligned
+    (dict(comb=None), _lib.SA_ERR_INVALID_ARG),
+    (dict(post=ctypes.c_void_p(1 << 41)), _lib.SA_ERR_INVALID_ARG),  # post overlaps pre
+    (dict(pre=ctypes.c_void_p((1 << 40) + 96)), _lib.SA_ERR_INVALID_ARG),  # pre inside mixes
+    (dict(n=0, mixes=None), _lib.SA_OK),
+])
+def test_hc_split_sinkhorn_rejects_bad_arguments(lib, kw, code):
+    assert _hc(lib, **kw) == code
+
