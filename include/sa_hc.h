@@ -29,7 +29,8 @@ extern "C" {
  *   comb[i]    = the hc x hc matrix a_{2 hc + j hc + k} (row j, column k; hc_scale[2]): each row
  *                replaced by its softmax plus eps, each column divided by (its sum + eps), then
  *                sinkhorn_iters - 1 rounds of dividing each row, then each column, by its sum + eps.
- * Everything in f32, as on the page (expf and IEEE division).
+ * Everything in f32, as on the page (expf, IEEE reciprocals; a normalisation multiplies by the
+ * reciprocal of its sum where the page divides, one rounding apart).
  *
  * Arguments
  *   mixes      f32 [n][(2 + hc) * hc], 16-byte aligned
