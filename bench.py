@@ -43,7 +43,9 @@ METRIC = ("sparse_attn query·heads/s and % of roofline (HBM GB/s decode, tensor
           "prefill)")
 UNIT = "query·heads/s"
 DEFAULT_WORKLOAD = "swa_prefill"
-FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+HBM_NOMINAL_GBS = 7900.0  # GB300 HBM3e, nominal (the roofline divides by the measured copy rate)
 L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 # A GPU-side spin (~0.2 ms at 2 GHz) after each flush, before the step's first event: the host
 # enqueues the whole step while the GPU spins, so the events time the step's kernels back to back
@@ -463,6 +465,36 @@ def time_hc_split_sinkhorn(dev, steps, warmup, peaks):
             "frac": round(gbs / peaks["hbm_gbs"], 4), "tokens": HC_TOKENS, "hc": 4, "iters": 20}
 
 
+def roofline_line(terms, peaks, ms_attn, traffic):
+    """The JSON line's roofline object for the sparse_attn call: the achieved rate against the
+    binding measured peak (HBM bytes or dense bf16 FLOPs), the other roofline beside it, and the
+    sustained-bf16 and nominal-HBM figures as context."""
+    t_attn = ms_attn / 1e3
+    gbs = terms["alg_bytes"] / t_attn / 1e9
+    tfs = terms["flops"] / t_attn / 1e12
+    hbm = {"unit": "GB/s", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+           "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    tc = {"unit": "TFLOP/s", "achieved": round(tfs, 1), "peak": peaks["bf16_tflops"],
+          "frac": round(tfs / peaks["bf16_tflops"], 4)}
+    binding, other = (hbm, tc) if terms["bound"] == "hbm" else (tc, hbm)
+    roof = {"bound": terms["bound"], "achieved": binding["achieved"], "peak": binding["peak"],
+            "unit": binding["unit"], "frac": binding["frac"], "traffic": traffic,
+            "kernel": "sa_sparse_attn", "ms": round(ms_attn, 4), "alg_bytes": terms["alg_bytes"],
+            "alg_flops": terms["flops"], "peak_source": peaks["source"] + " (burst)",
+            "other": other,
+            "roofline_ms": round(max(terms["t_hbm"], terms["t_tc"]) * 1e3, 4),
+            "frac_of_roofline_time": round(max(terms["t_hbm"], terms["t_tc"]) / t_attn, 4)}
+    # context beside the binding measured peak: the sustained bf16 figure (a long GEMM under the
+    # power cap) and the nominal HBM3e bandwidth
+    sustained = peaks.get("bf16_tflops_sustained")
+    roof["context"] = {
+        "bf16_tflops_sustained": sustained,
+        "tensor_frac_of_sustained": round(tfs / sustained, 4) if sustained else None,
+        "hbm_nominal_gbs": HBM_NOMINAL_GBS,
+        "hbm_frac_of_nominal": round(gbs / HBM_NOMINAL_GBS, 4)}
+    return roof
+
+
 def run_gpu(args, rank, world, local):
     import torch
     torch.cuda.set_device(local)
@@ -581,29 +613,9 @@ def run_gpu(args, rank, world, local):
     if not rank0:
         return None
     value = job_value(units, world, ms_step / 1e3)
-    bound = terms["bound"]
-    t_attn = ms_attn / 1e3
-    gbs = terms["alg_bytes"] / t_attn / 1e9
-    tfs = terms["flops"] / t_attn / 1e12
     lib_version = path.sa._lib.version()
     src_hash = kernel_source_hash()
-    traffic = NCU_TRAFFIC.get((src_hash, wl.name))
-    if bound == "hbm":
-        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic}
-        other = {"unit": "TFLOP/s", "achieved": round(tfs, 1), "peak": peaks["bf16_tflops"],
-                 "frac": round(tfs / peaks["bf16_tflops"], 4)}
-    else:
-        roof = {"bound": "tensor", "achieved": round(tfs, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(tfs / peaks["bf16_tflops"], 4),
-                "traffic": traffic}
-        other = {"unit": "GB/s", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                 "frac": round(gbs / peaks["hbm_gbs"], 4)}
-    roof.update({"kernel": "sa_sparse_attn", "ms": round(ms_attn, 4),
-                 "alg_bytes": terms["alg_bytes"], "alg_flops": terms["flops"],
-                 "peak_source": peaks["source"] + " (burst)", "other": other,
-                 "roofline_ms": round(max(terms["t_hbm"], terms["t_tc"]) * 1e3, 4),
-                 "frac_of_roofline_time": round(max(terms["t_hbm"], terms["t_tc"]) / t_attn, 4)})
+    roof = roofline_line(terms, peaks, ms_attn, NCU_TRAFFIC.get((src_hash, wl.name)))
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),

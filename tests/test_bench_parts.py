@@ -35,3 +35,27 @@ def test_parts_cover_every_query_once(b, s, n):
     edges = [p[0][dim] for p in parts]
     assert edges[0].start == 0 and edges[-1].stop == (b if b > 1 else s)
     assert all(x.stop == y.start for x, y in zip(edges, edges[1:]))
+
+
+def test_roofline_line_binding_and_context():
+    import bench
+    peaks = {"hbm_gbs": 6659.6, "bf16_tflops": 1922.9, "bf16_tflops_sustained": 1731.3,
+             "source": "measured"}
+    # an HBM-bound call: 541.1 MB and 68.7 GFLOP in 0.1308 ms
+    terms = {"bound": "hbm", "alg_bytes": 541_065_216, "flops": 68_719_476_736.0,
+             "t_hbm": 541_065_216 / 6659.6e9, "t_tc": 68_719_476_736.0 / 1922.9e12}
+    r = bench.roofline_line(terms, peaks, 0.1308, 500_166_656)
+    gbs = 541_065_216 / 0.1308e-3 / 1e9
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["traffic"] == 500_166_656
+    assert abs(r["achieved"] - gbs) < 0.1 and abs(r["frac"] - gbs / 6659.6) < 1e-4
+    assert r["other"]["unit"] == "TFLOP/s"
+    assert abs(r["frac_of_roofline_time"] - terms["t_hbm"] / 0.1308e-3) < 1e-4
+    assert abs(r["context"]["hbm_frac_of_nominal"] - gbs / bench.HBM_NOMINAL_GBS) < 1e-4
+    # a tensor-bound call; the fallback peaks carry a sustained figure too
+    terms = {"bound": "tensor", "alg_bytes": 1e9, "flops": 6.87e14, "t_hbm": 1e9 / 6.8e12,
+             "t_tc": 6.87e14 / 1.9e15}
+    r = bench.roofline_line(terms, dict(bench.FALLBACK_PEAKS), 1.121, None)
+    tfs = 6.87e14 / 1.121e-3 / 1e12
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["traffic"] is None
+    assert abs(r["frac"] - tfs / 1900.0) < 1e-4 and r["peak_source"] == "fallback (burst)"
+    assert abs(r["context"]["tensor_frac_of_sustained"] - tfs / 1700.0) < 1e-4
