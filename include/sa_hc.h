@@ -19,9 +19,9 @@ extern "C" {
 /*
  * hc_split_sinkhorn.
  *
- * Source: "DeepSeek V4.1" attention page, hc_split_sinkhorn and its kernel (the block's mixes
- * split into pre / post weights and a Sinkhorn-normalised comb matrix); the model config
- * (hc_mult 4, hc_sinkhorn_iters 20, hc_eps 1e-6).
+ * Source: "DeepSeek V4.1" attention-write page (decode), hc_split_sinkhorn and its kernel (the block's mixes
+ * split into pre / post weights and a Sinkhorn-normalised comb matrix); the model config on the
+ * "DeepSeek V4.1" first-layer attention update page (hc_mult 4, hc_sinkhorn_iters 20, hc_eps 1e-6).
  *
  * For every token i < n, with a_j = mixes[i][j] * hc_scale[.] + hc_base[j] in f32:
  *   pre[i][j]  = sigmoid(a_j) + eps              (hc_scale[0], j < hc)

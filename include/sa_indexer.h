@@ -27,7 +27,7 @@ typedef enum {
 /*
  * The indexer's selection of the compressed idx.
  *
- * Source: "DeepSeek V4.1" attention page, Indexer.forward (the steps after the index scores are
+ * Source: "DeepSeek V4.1" source-layer attention page (indexer view), Indexer.forward (the steps after the index scores are
  * formed: the visibility mask of a prefill, the level-two candidate mask of a layer that uses
  * another layer's candidate blocks, topk, the sort into position order, and the
  * unreachable -> -1 / offset rule).
@@ -64,7 +64,7 @@ sa_status sa_indexer_topk(const void* score, int score_format, const uint8_t* ca
 /*
  * Level one of the two-level top-k: the candidate blocks.
  *
- * Source: "DeepSeek V4.1" attention page, select_candidate_blocks (and Indexer.forward, which
+ * Source: "DeepSeek V4.1" source-layer attention page (indexer view), select_candidate_blocks (and Indexer.forward, which
  * calls it on the masked index scores of the candidate-source layer with its compress_lens).
  *
  * For every sequence bi and query si, with visible as for sa_indexer_topk (positions at or past

@@ -8,8 +8,10 @@ first use and marshals numpy arrays through ctypes.
 
 Sources (see the header of ``sa_oracle.c``): the "Module attn" API page of the spark_model
 deepseek_v41_ref docs (precision paragraph, ring-cache paragraph, act_quant_inplace, pow2_ceil,
-sparse_attn, window_topk_idxs) and the "DeepSeek V4.1" Attention.forward / __init__ pages
-(Indexer.forward for the selection of the compressed idx).
+sparse_attn, window_topk_idxs), the "DeepSeek V4.1" attention output page (Attention.forward /
+__init__, apply_rotary_emb), its source-layer attention page in the indexer view
+(Indexer.forward's selection, select_candidate_blocks) and its attention-write page
+(hc_split_sinkhorn).
 """
 
 from __future__ import annotations

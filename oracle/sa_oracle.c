@@ -12,11 +12,13 @@
  *   [FWD]  "DeepSeek V4.1" attention page (attention/output, prefill): Attention.forward and
  *          Attention.__init__ (softmax_scale = head_dim ** -0.5, attn_sink per local head),
  *          apply_rotary_emb (the inverse rotation of the output's rope dims).
- *   [IDX]  the same page, Indexer.forward: the selection that turns index scores into the
- *          compressed idx (visibility mask, top-k, position sort, -1 / offset).
- *   [CAND] the same page, select_candidate_blocks: level one of the two-level top-k.
- *   [HC]   the same page, hc_split_sinkhorn (and its kernel): a Hyper-Connections block's mixes
- *          split into pre / post weights and a Sinkhorn-normalised comb matrix.
+ *   [IDX]  "DeepSeek V4.1" source-layer attention page (indexer view), Indexer.forward: the
+ *          selection that turns index scores into the compressed idx (visibility mask, top-k,
+ *          position sort, -1 / offset).
+ *   [CAND] the same indexer page, select_candidate_blocks: level one of the two-level top-k.
+ *   [HC]   "DeepSeek V4.1" attention-write page (decode), hc_split_sinkhorn (and its kernel): a
+ *          Hyper-Connections block's mixes split into pre / post weights and a
+ *          Sinkhorn-normalised comb matrix.
  *
  * Floating point: dot products, the softmax and the weighted sum are carried in f64; the only
  * rounding to a narrow type is the final bf16 round-to-nearest-even of o.  The act_quant steps

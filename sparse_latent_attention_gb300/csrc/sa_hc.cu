@@ -1,4 +1,4 @@
-// hc_split_sinkhorn ("DeepSeek V4.1" attention page): a Hyper-Connections block's per-token mixes
+// hc_split_sinkhorn ("DeepSeek V4.1" attention-write page (decode)): a Hyper-Connections block's per-token mixes
 // split into pre / post weights and a Sinkhorn-normalised comb matrix, and its C ABI entry
 // (include/sa_hc.h).
 //

@@ -1,4 +1,4 @@
-// The indexer's two selection steps ("DeepSeek V4.1" attention page) and their C ABI entries
+// The indexer's two selection steps ("DeepSeek V4.1" source-layer attention page (indexer view)) and their C ABI entries
 // (include/sa_indexer.h):
 //   indexer_topk_kernel      Indexer.forward after the scores: visibility mask, the optional
 //                            level-two candidate mask, topk, sort into position order,

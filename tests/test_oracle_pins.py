@@ -473,7 +473,7 @@ def test_rope_rejects_bad_arguments():
 
 
 # --------------------------------------------------------------------------------------------
-# the indexer's selection ("DeepSeek V4.1" attention page, Indexer.forward)
+# the indexer's selection ("DeepSeek V4.1" source-layer attention page (indexer view), Indexer.forward)
 # --------------------------------------------------------------------------------------------
 
 def _golden_indexer():
@@ -571,7 +571,7 @@ def test_indexer_topk_bf16_scores_and_bad_arguments():
 
 
 # --------------------------------------------------------------------------------------------
-# select_candidate_blocks ("DeepSeek V4.1" attention page)
+# select_candidate_blocks ("DeepSeek V4.1" source-layer attention page (indexer view))
 # --------------------------------------------------------------------------------------------
 
 def _golden_candidates():
@@ -651,7 +651,7 @@ def test_candidate_blocks_invariants_and_level_two():
 
 
 # --------------------------------------------------------------------------------------------
-# hc_split_sinkhorn ("DeepSeek V4.1" attention page)
+# hc_split_sinkhorn ("DeepSeek V4.1" attention-write page (decode))
 # --------------------------------------------------------------------------------------------
 
 def _hc_case(seed, n=64, hc=4, spread=1.0):
