@@ -12,7 +12,10 @@ launching stream, and queued whole before its first event fires); `e2e` times th
 copied from pinned host memory and the output read back, the queries in parts (--e2e-chunks)
 whose copies in and out overlap the attention of other parts.  `roofline` relates the sparse_attn
 launch to the binding roofline (HBM bytes or dense bf16 FLOPs), and `cpu_baseline` times the CPU
-oracle on a bounded sample of the same workload.
+oracle on a bounded sample of the same workload.  The headline workload is the largest one that
+fits one GPU (the window + compressed prefill); `workloads` adds the device timing and roofline
+fraction of every timed workload (sliding-window prefill, window + compressed prefill, batched
+decode, fp8-kv long decode), each run the same way.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -42,7 +45,9 @@ from sparse_latent_attention_gb300 import workloads  # noqa: E402
 METRIC = ("sparse_attn query·heads/s and % of roofline (HBM GB/s decode, tensor-pipe "
           "prefill)")
 UNIT = "query·heads/s"
-DEFAULT_WORKLOAD = "swa_prefill"
+DEFAULT_WORKLOAD = "cmp_prefill"  # the largest single-GPU workload (most FLOPs and bytes)
+# every workload the line times besides the headline one (the tiny case is parity-only)
+TIMED_WORKLOADS = ("swa_prefill", "cmp_prefill", "decode", "fp8_decode")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "source": "fallback"}
 HBM_NOMINAL_GBS = 7900.0  # GB300 HBM3e, nominal (the roofline divides by the measured copy rate)
@@ -195,10 +200,10 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0: float, t1: float):
+    def summary(self, t0: float, t1: float, widen: bool = True):
         inside = [p for t, p in self.samples if t0 <= t <= t1]
-        window = "timed region"
-        if len(inside) < 3:  # a short timed region: widen to the run around it
+        window = "timed region" if widen else "every timed step of every workload"
+        if len(inside) < 3 and widen:  # a short timed region: widen to the run around it
             inside = [p for t, p in self.samples]
             window = "warm-up + timed run"
         if not inside:
@@ -495,6 +500,100 @@ def roofline_line(terms, peaks, ms_attn, traffic):
     return roof
 
 
+def time_device_steps(torch, path, flush, steps, warmup):
+    """warmup + steps passes of the path, each timed on the device with CUDA events (the step, and
+    the sparse_attn call inside it); the L2 is flushed before every step and the step is queued
+    whole behind an untimed GPU spin, so the events time the kernels back to back."""
+    for _ in range(warmup):
+        flush.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)
+        path.step()
+    torch.cuda.synchronize()
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(steps)]
+    for e in ev:
+        flush.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)  # not timed: lets the host queue the step first
+        e[0].record()
+        path.step(ev=(e[2], e[3]))
+        e[1].record()
+    torch.cuda.synchronize()
+    return ([a.elapsed_time(b) for a, b, _, _ in ev], [c.elapsed_time(d) for _, _, c, d in ev])
+
+
+def config_of(wl, world, rope=0):
+    """The workload's config object; the GPU arm and the reference arm print the same one."""
+    return {"workload": wl.name, "b": wl.b, "s": wl.s, "h": wl.h, "d": wl.d,
+            "rows": wl.rows, "topk": wl.topk, "window": wl.window,
+            "start_pos": wl.start_pos, "kv_format": wl.kv_format,
+            "l2": "flushed between timed steps (256 MB write, outside the step events)",
+            "launch": "each step fully queued before its first event (a 0.2 ms GPU spin "
+                      "after the flush, outside the events)",
+            "parallelism": f"replica x{world}" if world > 1 else "1 GPU",
+            **({"inverse_rope_dims": rope} if rope else {})}
+
+
+def workload_line(wl, terms, peaks, step_ms, attn_ms, traffic):
+    """One workload's device timing: the step and its sparse_attn call, the binding roofline's
+    fraction, the other roofline, and the ncu traffic for the current kernel sources (or null)."""
+    ms_step = sum(step_ms) / len(step_ms)
+    ms_attn = sum(attn_ms) / len(attn_ms)
+    roof = roofline_line(terms, peaks, ms_attn, traffic)
+    return {"ms_per_step": round(ms_step, 4), "ms_attn": round(ms_attn, 4),
+            "value": round(wl.n_tokens * wl.h / (ms_step / 1e3), 1), "unit": UNIT,
+            "bound": roof["bound"], "frac": roof["frac"], "achieved": roof["achieved"],
+            "peak": roof["peak"], "roof_unit": roof["unit"], "other": roof["other"],
+            "roofline_ms": roof["roofline_ms"], "traffic": traffic,
+            "traffic_key": [kernel_source_hash(), wl.name], "steps": len(step_ms)}
+
+
+def host_link_rates(torch, dev, nbytes=256 << 20, reps=5):
+    """Pinned host <-> device copy rates (GB/s, best of reps), each direction alone and both at
+    once on two streams: the floor of the end-to-end step's copies."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def best(fn):
+        t = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b) / 1e3)
+        return min(t)
+
+    def both():
+        cur = torch.cuda.current_stream()
+        s1.wait_stream(cur)
+        s2.wait_stream(cur)
+        with torch.cuda.stream(s1):
+            d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+        cur.wait_stream(s1)
+        cur.wait_stream(s2)
+
+    t_h2d = best(lambda: d.copy_(h, non_blocking=True))
+    t_d2h = best(lambda: h2.copy_(d2, non_blocking=True))
+    t_both = best(both)
+    return {"h2d_gbs": round(nbytes / t_h2d / 1e9, 1), "d2h_gbs": round(nbytes / t_d2h / 1e9, 1),
+            "duplex_gbs": round(2 * nbytes / t_both / 1e9, 1), "bytes": nbytes}
+
+
+def e2e_link_floor_ms(link, h2d_bytes, d2h_bytes):
+    """The end-to-end step's copies alone at the measured pinned rates, the two directions
+    overlapped (as the step's parts overlap them): max of each direction alone and of the total
+    at the duplex rate."""
+    t = max(h2d_bytes / (link["h2d_gbs"] * 1e9), d2h_bytes / (link["d2h_gbs"] * 1e9),
+            (h2d_bytes + d2h_bytes) / (link["duplex_gbs"] * 1e9))
+    return t * 1e3
+
+
 def run_gpu(args, rank, world, local):
     import torch
     torch.cuda.set_device(local)
@@ -510,30 +609,15 @@ def run_gpu(args, rank, world, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     sampler = ClockSampler(gpu_id_of(torch, dev)).start() if rank0 else None
-    for _ in range(args.warmup):
-        flush.zero_()
-        torch.cuda._sleep(HEAD_START_CYCLES)
-        path.step()
-    torch.cuda.synchronize()
+    time_device_steps(torch, path, flush, 0, args.warmup)
 
     # timed region: K steps, each bracketed by events; L2 flushed between steps (not timed)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
-    for e in ev:
-        flush.zero_()
-        torch.cuda._sleep(HEAD_START_CYCLES)  # not timed: lets the host queue the step first
-        e[0].record()
-        path.step(ev=(e[2], e[3]))
-        e[1].record()
-    torch.cuda.synchronize()
+    step_ms, attn_ms = time_device_steps(torch, path, flush, args.steps, 0)
     barrier(world)
     t1 = time.time()
-    step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
-    attn_ms = [c.elapsed_time(d) for _, _, c, d in ev]
     assert path.sa.read_status(path.ws) == 0, "kernel reported an out-of-range index"
 
     # end to end through the public API: host inputs in, host output out, every step
@@ -603,8 +687,32 @@ def run_gpu(args, rank, world, local):
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # the other workloads, each timed alone the same way (device time only; rank 0's GPU line
+    # carries them, every rank runs them so the ranks stay in step)
+    others = {}
+    if not args.headline_only and args.batch is None:
+        del flush
+        for name in TIMED_WORKLOADS:
+            if name == wl.name:
+                continue
+            wl_o = workloads.make_named(name)
+            path_o = GpuPath(wl_o, dev)
+            path_o.step()
+            torch.cuda.synchronize()
+            terms_o = roofline_terms(wl_o, path_o.idx.cpu().numpy(), peaks)
+            flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+            time_device_steps(torch, path_o, flush, 0, args.warmup)
+            sm_o, am_o = time_device_steps(torch, path_o, flush, args.steps, 0)
+            assert path_o.sa.read_status(path_o.ws) == 0, f"{name}: kernel status"
+            others[name] = workload_line(wl_o, terms_o, peaks, sm_o, am_o,
+                                         NCU_TRAFFIC.get((kernel_source_hash(), name)))
+            del path_o, flush
+            torch.cuda.empty_cache()
+    t2 = time.time()
     if sampler:
         sampler.stop()
+    link = host_link_rates(torch, dev) if rank0 else None
 
     units = wl.n_tokens * wl.h
     ms_step = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
@@ -623,20 +731,19 @@ def run_gpu(args, rank, world, local):
         "dtype": "fp8-e4m3 kv, bf16 q/o, f32 accumulate" if path.fp8 else
                  "bf16 (f32 accumulate)",
         "data": "synthetic (seeded N(0,1) inputs with the workload's index structure)",
-        "config": {"workload": wl.name, "b": wl.b, "s": wl.s, "h": wl.h, "d": wl.d,
-                   "rows": wl.rows, "topk": wl.topk, "window": wl.window,
-                   "start_pos": wl.start_pos, "kv_format": wl.kv_format,
-                   "l2": "flushed between timed steps (256 MB write, outside the step events)",
-                   "launch": "each step fully queued before its first event (a 0.2 ms GPU spin "
-                             "after the flush, outside the events)",
-                   "parallelism": f"replica x{world}" if world > 1 else "1 GPU",
-                   **({"inverse_rope_dims": args.rope} if args.rope else {})},
+        "config": config_of(wl, world, args.rope),
         "roofline": roof,
         "e2e": {"value": round(job_value(units, world, ms_e2e / 1e3), 1), "unit": UNIT,
                 "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "parts": len(parts)},
+                "d2h_bytes_per_step": int(d2h), "parts": len(parts),
+                "link": link,
+                "link_floor_ms": round(e2e_link_floor_ms(link, h2d, d2h), 4),
+                "frac_of_link_floor": round(e2e_link_floor_ms(link, h2d, d2h) / ms_e2e, 4)},
         "gpu_launches": path.launches_per_step * args.steps,
         "clocks": sampler.summary(t0, t1) if sampler else None,
+        "clocks_all_timing": sampler.summary(t0, t2, widen=False) if sampler else None,
+        "workloads": dict(others, **{wl.name: workload_line(
+            wl, terms, peaks, step_ms, attn_ms, NCU_TRAFFIC.get((src_hash, wl.name)))}),
         "lib_version": lib_version,
         "kernel_source_hash": src_hash,
         "library_source_hash": library_source_hash(),
@@ -782,11 +889,11 @@ def run_reference(args, rank, world):
         "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
         "data": "synthetic (seeded N(0,1) inputs with the workload's index structure)",
-        "config": {"workload": wl.name, "b": wl.b, "s": wl.s, "h": wl.h, "d": wl.d,
-                   "rows": wl.rows, "topk": wl.topk, "tokens_per_step": n},
+        "config": config_of(wl, world),
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "kind": "oracle",
                          "cores": step.threads,
-                         "sample": f"{n} query tokens per step (all heads) of {wl.name}"},
+                         "sample": f"{n} query tokens per step (all heads) of {wl.name}, "
+                                   "with the step's window_idxs and act_quant"},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -803,6 +910,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only --workload (skip the line's other workloads)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences of a decode workload (a smaller case for profiler captures)")
     ap.add_argument("--e2e-chunks", type=int, default=0,

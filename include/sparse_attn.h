@@ -43,6 +43,13 @@ typedef enum {
     SA_KV_FP8_E4M3 = 1       /* kv is e4m3 [b][rows][d] + kv_scale e8m0 [b][rows][d/32] */
 } sa_kv_format;
 
+/* Which kernel family computes sparse_attn (sa_sparse_attn_family). */
+typedef enum {
+    SA_FAMILY_AUTO = 0,      /* what sa_sparse_attn uses: tcgen05 for head_dim 512, else mma.sync */
+    SA_FAMILY_TCGEN05 = 1,   /* the tcgen05 / TMEM kernels; head_dim 512 only */
+    SA_FAMILY_MMA_SYNC = 2   /* the warp-level mma.sync kernels; every supported head_dim */
+} sa_kernel_family;
+
 /* Status word block at the start of every workspace, in bytes. */
 #define SA_STATUS_BYTES 256
 
@@ -85,6 +92,18 @@ sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale,
                          void* o, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sa_sparse_attn computed by a chosen kernel family (sa_kernel_family), e.g. to compare the two
+ * families on the same inputs.  Same source, arguments, result and workspace size as
+ * sa_sparse_attn; SA_FAMILY_AUTO is exactly sa_sparse_attn.  SA_FAMILY_TCGEN05 with a head_dim
+ * other than 512 returns SA_ERR_UNSUPPORTED; any other family value SA_ERR_INVALID_ARG.
+ */
+sa_status sa_sparse_attn_family(const void* q, const void* kv, const uint8_t* kv_scale,
+                                int kv_format, const float* sink, const int32_t* idx,
+                                float softmax_scale, int64_t b, int64_t s, int h, int d,
+                                int64_t rows, int topk, void* o, void* workspace,
+                                size_t workspace_bytes, int family, void* stream);
+
+/*
  * sparse_attn with the inverse rotary embedding of the output fused in.
  *
  * Source: "DeepSeek V4.1" attention page, Attention.forward (after sparse_attn, the last
@@ -107,7 +126,7 @@ sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale,
  *   rope_dim   even, 2 <= rope_dim <= d
  *   start_pos  position of token 0 of every sequence (the prefill's 0, a decode step's length)
  * Supported: d = 512 (the tcgen05 kernel family, which fuses the rotation into its epilogue);
- * other head dims, or SA_FORCE_MMA=1 in the environment, return SA_ERR_UNSUPPORTED.
+ * other head dims return SA_ERR_UNSUPPORTED.
  */
 sa_status sa_sparse_attn_rope(const void* q, const void* kv, const uint8_t* kv_scale,
                               int kv_format, const float* sink, const int32_t* idx,
@@ -116,8 +135,9 @@ sa_status sa_sparse_attn_rope(const void* q, const void* kv, const uint8_t* kv_s
                               size_t workspace_bytes, const float* rot, int64_t npos, int rope_dim,
                               int64_t start_pos, void* stream);
 
-/* Workspace bytes sa_sparse_attn needs for this shape (always >= SA_STATUS_BYTES).  Returns 0
- * for an unsupported shape. */
+/* Workspace bytes sa_sparse_attn needs for this shape (always >= SA_STATUS_BYTES), enough for
+ * either kernel family and any GPU: a pure function of the arguments.  Returns 0 for an
+ * unsupported shape. */
 size_t sa_sparse_attn_workspace_size(int64_t b, int64_t s, int h, int d, int64_t rows, int topk,
                                      int kv_format);
 
@@ -134,15 +154,15 @@ size_t sa_sparse_attn_workspace_size(int64_t b, int64_t s, int h, int d, int64_t
  * workspace, which is replaced by a SA_STATIC_SCRATCH_BYTES array that the library keeps in
  * device memory on every GPU that loads it, until the process exits.  Allocates nothing.
  *   status_out  optional device uint32: receives the call's status word (bit 0 set when an index
- *               outside [-1, rows) was seen); NULL to skip.  The word is cleared at the start of
- *               every call.
+ *               outside [-1, rows) was seen, bit 1 when a kernel wait gave up, in which case o is
+ *               not valid); NULL to skip.  The word is cleared at the start of every call; a call
+ *               with b * s == 0 writes 0 to it.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
  * that device current) and caches it: make that first call before any stream capture.  Every call
  * shares the one array, which keeps the last call's contents; calls whose work overlaps on the
  * GPU (unordered streams) race on it and must be serialised by the caller.
- * Returns SA_ERR_WORKSPACE when the shape needs more scratch than SA_STATIC_SCRATCH_BYTES (only
- * few-token calls with many idx columns need more than the status word), otherwise as
- * sa_sparse_attn.
+ * Returns SA_ERR_WORKSPACE when the kernel family the call runs in (as sa_sparse_attn routes it)
+ * needs more scratch than SA_STATIC_SCRATCH_BYTES for this shape, otherwise as sa_sparse_attn.
  */
 sa_status sa_sparse_attn_static_scratch(const void* q, const void* kv, const uint8_t* kv_scale,
                                         int kv_format, const float* sink, const int32_t* idx,

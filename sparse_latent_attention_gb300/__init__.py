@@ -59,14 +59,19 @@ def new_workspace(b, s, h, d, rows, topk, kv_format=SA_KV_BF16, device="cuda") -
                        device=device)
 
 
+FAMILIES = {"auto": _lib.SA_FAMILY_AUTO, "tcgen05": _lib.SA_FAMILY_TCGEN05,
+            "mma": _lib.SA_FAMILY_MMA_SYNC}
+
+
 def sparse_attn(q, kv, sink, idx, softmax_scale, *, kv_scale=None, out=None, workspace=None,
-                rope=None, stream=None) -> torch.Tensor:
+                rope=None, family=None, stream=None) -> torch.Tensor:
     """o[b, s, h, d] (bf16) = sparse_attn(q, kv, sink, idx, softmax_scale).
 
     q [b, s, h, d] bf16; kv [b, rows, d] bf16, or uint8 e4m3 codes with kv_scale [b, rows, d/32]
     uint8 e8m0; sink [h] f32; idx [b, s, topk] int32 (-1 = empty).
     rope=(rot, start_pos): also rotate o's last rot.shape[1] * 2 dims back by the inverse rotary
-    embedding of positions start_pos + si, rot [positions, rope_dim / 2, 2] f32 (cos, sin)."""
+    embedding of positions start_pos + si, rot [positions, rope_dim / 2, 2] f32 (cos, sin).
+    family: None (= "auto"), "tcgen05" or "mma" -- the kernel family that computes the call."""
     _need(q, "q", torch.bfloat16)
     dev = q.device
     b, s, h, d = q.shape
@@ -96,7 +101,11 @@ def sparse_attn(q, kv, sink, idx, softmax_scale, *, kv_scale=None, out=None, wor
         workspace = new_workspace(b, s, h, d, rows, topk, fmt, device=dev)
     else:
         _need(workspace, "workspace", torch.uint8, dev)
+    if family is not None and family not in FAMILIES:
+        raise ValueError(f"family must be one of {sorted(FAMILIES)}")
     if rope is not None:
+        if family not in (None, "auto", "tcgen05"):
+            raise ValueError("the fused rotation runs in the tcgen05 family only")
         rot, start_pos = rope
         _need(rot, "rot", torch.float32, dev)
         if rot.dim() != 3 or rot.shape[2] != 2:
@@ -107,6 +116,13 @@ def sparse_attn(q, kv, sink, idx, softmax_scale, *, kv_scale=None, out=None, wor
                                         rot.shape[0], 2 * rot.shape[1], int(start_pos),
                                         _stream(stream))
         _lib.check(st, "sa_sparse_attn_rope")
+        return out
+    if family is not None:
+        st = load().sa_sparse_attn_family(_ptr(q), _ptr(kv), _ptr(kv_scale), fmt, _ptr(sink),
+                                          _ptr(idx), float(softmax_scale), b, s, h, d, rows, topk,
+                                          _ptr(out), _ptr(workspace), workspace.numel(),
+                                          FAMILIES[family], _stream(stream))
+        _lib.check(st, "sa_sparse_attn_family")
         return out
     st = load().sa_sparse_attn(_ptr(q), _ptr(kv), _ptr(kv_scale), fmt, _ptr(sink), _ptr(idx),
                                float(softmax_scale), b, s, h, d, rows, topk, _ptr(out),

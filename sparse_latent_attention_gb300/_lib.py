@@ -20,6 +20,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "sparse_attn.h")
 (SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_INDEX, SA_ERR_WORKSPACE,
  SA_ERR_TIMEOUT) = range(7)
 SA_KV_BF16, SA_KV_FP8_E4M3 = 0, 1
+SA_FAMILY_AUTO, SA_FAMILY_TCGEN05, SA_FAMILY_MMA_SYNC = 0, 1, 2
 SA_SCORE_F32, SA_SCORE_BF16 = 0, 1
 SA_INDEXER_MAX_POSITIONS = 49152
 SA_STATUS_BYTES = 256
@@ -50,6 +51,9 @@ def load() -> ctypes.CDLL:
         lib.sa_sparse_attn.restype = i32
         lib.sa_sparse_attn.argtypes = [P, P, P, i32, P, P, f32, i64, i64, i32, i32, i64, i32, P, P,
                                        sz, P]
+        lib.sa_sparse_attn_family.restype = i32
+        lib.sa_sparse_attn_family.argtypes = [P, P, P, i32, P, P, f32, i64, i64, i32, i32, i64, i32,
+                                              P, P, sz, i32, P]
         lib.sa_sparse_attn_rope.restype = i32
         lib.sa_sparse_attn_rope.argtypes = [P, P, P, i32, P, P, f32, i64, i64, i32, i32, i64, i32,
                                             P, P, sz, P, i64, i32, i64, P]

@@ -3,7 +3,6 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
-#include <stdlib.h>
 
 #include "sa_internal.cuh"
 #include "sparse_attn.h"
@@ -31,21 +30,35 @@ bool supported_shape(int64_t b, int64_t s, int h, int d, int64_t rows, int topk)
 
 sa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SA_OK : SA_ERR_CUDA; }
 
-// SA_FORCE_MMA=1 in the environment routes every call to the mma.sync kernels (used to compare
-// the two kernel families on the same inputs); read on every call.
-bool force_mma() {
-    const char* v = getenv("SA_FORCE_MMA");
-    return v && v[0] == '1';
-}
-
 // The whole sparse_attn call; rope == nullptr for none (checked by the caller).
 sa_status attn_call(const void* q, const void* kv, const uint8_t* kv_scale, int kv_format,
                     const float* sink, const int32_t* idx, float softmax_scale, int64_t b, int64_t s,
                     int h, int d, int64_t rows, int topk, void* o, void* workspace,
                     size_t workspace_bytes, const float* rope, int rope_dim, int64_t rope_pos0,
-                    void* stream);
+                    int family, void* stream);
 
 }  // namespace
+
+namespace sa {
+
+// The family a call runs in (SA_FAMILY_AUTO resolved), or -1 when the requested one cannot run
+// this shape.
+int routed_family(int family, int h, int d, int kv_format, int64_t b, int64_t rows) {
+    const bool tc = attn_tc_supports(h, d, kv_format, b, rows);
+    if (family == SA_FAMILY_AUTO) return tc ? SA_FAMILY_TCGEN05 : SA_FAMILY_MMA_SYNC;
+    if (family == SA_FAMILY_TCGEN05) return tc ? SA_FAMILY_TCGEN05 : -1;
+    if (family == SA_FAMILY_MMA_SYNC) return SA_FAMILY_MMA_SYNC;
+    return -1;
+}
+
+size_t routed_workspace_bytes(int family, int64_t b, int64_t s, int h, int d, int64_t rows,
+                              int topk) {
+    const size_t scratch = family == SA_FAMILY_TCGEN05 ? attn_tc_scratch_bytes(b, s, h, topk)
+                                                       : attn_mma_scratch_bytes(b, s, h, d, topk);
+    return SA_STATUS_BYTES + align_up(scratch, 256);
+}
+
+}  // namespace sa
 
 extern "C" {
 
@@ -67,7 +80,18 @@ sa_status sa_sparse_attn(const void* q, const void* kv, const uint8_t* kv_scale,
                          int64_t b, int64_t s, int h, int d, int64_t rows, int topk,
                          void* o, void* workspace, size_t workspace_bytes, void* stream) {
     return attn_call(q, kv, kv_scale, kv_format, sink, idx, softmax_scale, b, s, h, d, rows, topk,
-                     o, workspace, workspace_bytes, nullptr, 0, 0, stream);
+                     o, workspace, workspace_bytes, nullptr, 0, 0, SA_FAMILY_AUTO, stream);
+}
+
+sa_status sa_sparse_attn_family(const void* q, const void* kv, const uint8_t* kv_scale,
+                                int kv_format, const float* sink, const int32_t* idx,
+                                float softmax_scale, int64_t b, int64_t s, int h, int d,
+                                int64_t rows, int topk, void* o, void* workspace,
+                                size_t workspace_bytes, int family, void* stream) {
+    if (family != SA_FAMILY_AUTO && family != SA_FAMILY_TCGEN05 && family != SA_FAMILY_MMA_SYNC)
+        return SA_ERR_INVALID_ARG;
+    return attn_call(q, kv, kv_scale, kv_format, sink, idx, softmax_scale, b, s, h, d, rows, topk,
+                     o, workspace, workspace_bytes, nullptr, 0, 0, family, stream);
 }
 
 sa_status sa_sparse_attn_rope(const void* q, const void* kv, const uint8_t* kv_scale,
@@ -81,13 +105,14 @@ sa_status sa_sparse_attn_rope(const void* q, const void* kv, const uint8_t* kv_s
     if (start_pos > npos - s) return SA_ERR_INVALID_ARG;  // positions start_pos .. start_pos + s - 1
     if (kv_format != SA_KV_BF16 && kv_format != SA_KV_FP8_E4M3) return SA_ERR_INVALID_ARG;
     // the rotation is fused into the tcgen05 kernel's epilogue only
-    if (!sa::attn_tc_supports(h, d, kv_format, b, rows) || force_mma()) return SA_ERR_UNSUPPORTED;
+    if (!sa::attn_tc_supports(h, d, kv_format, b, rows)) return SA_ERR_UNSUPPORTED;
     if (b * s > 0 && (!rot || !aligned(rot, 8))) return SA_ERR_INVALID_ARG;
     if (b * s > 0 && overlaps(o, (size_t)(b * s) * h * (size_t)d * 2, rot,
                               (size_t)npos * rope_dim * sizeof(float)))
         return SA_ERR_INVALID_ARG;
     return attn_call(q, kv, kv_scale, kv_format, sink, idx, softmax_scale, b, s, h, d, rows, topk,
-                     o, workspace, workspace_bytes, rot, rope_dim, start_pos, stream);
+                     o, workspace, workspace_bytes, rot, rope_dim, start_pos, SA_FAMILY_TCGEN05,
+                     stream);
 }
 
 }  // extern "C"
@@ -98,10 +123,12 @@ sa_status attn_call(const void* q, const void* kv, const uint8_t* kv_scale, int 
                     const float* sink, const int32_t* idx, float softmax_scale, int64_t b, int64_t s,
                     int h, int d, int64_t rows, int topk, void* o, void* workspace,
                     size_t workspace_bytes, const float* rope, int rope_dim, int64_t rope_pos0,
-                    void* stream) {
+                    int family, void* stream) {
     if (kv_format != SA_KV_BF16 && kv_format != SA_KV_FP8_E4M3) return SA_ERR_INVALID_ARG;
     if (b < 0 || s < 0 || h < 1 || d < 1 || rows < 0 || topk < 0) return SA_ERR_INVALID_ARG;
     if (!supported_shape(b, s, h, d, rows, topk)) return SA_ERR_UNSUPPORTED;
+    const int fam = sa::routed_family(family, h, d, kv_format, b, rows);
+    if (fam < 0) return SA_ERR_UNSUPPORTED;
     if (kv_format == SA_KV_BF16 && kv_scale) return SA_ERR_INVALID_ARG;
     if (b * s == 0) return SA_OK;  // nothing to compute; pointers of empty tensors may be NULL
     // kv (and kv_scale) may be NULL only when there are no rows, idx only when topk == 0
@@ -110,17 +137,20 @@ sa_status attn_call(const void* q, const void* kv, const uint8_t* kv_scale, int 
     if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(o, 16) || !aligned(sink, 4) ||
         !aligned(idx, 4))
         return SA_ERR_INVALID_ARG;
-    const size_t need = sa_sparse_attn_workspace_size(b, s, h, d, rows, topk, kv_format);
-    if (!workspace || workspace_bytes < need) return SA_ERR_WORKSPACE;
-    if (!aligned(workspace, 256)) return SA_ERR_INVALID_ARG;
     const size_t n_tok = (size_t)(b * s);
     const size_t o_bytes = n_tok * h * (size_t)d * 2;
     const size_t kv_bytes = (size_t)b * rows * d * (kv_format == SA_KV_BF16 ? 2 : 1);
+    // every argument other than the workspace is checked before the workspace is looked at, so a
+    // call without one validates the others (and enqueues nothing)
     if (overlaps(o, o_bytes, q, o_bytes) || overlaps(o, o_bytes, kv, kv_bytes) ||
         overlaps(o, o_bytes, idx, n_tok * topk * 4) || overlaps(o, o_bytes, sink, h * 4) ||
-        overlaps(o, o_bytes, workspace, need) ||
         (kv_scale && overlaps(o, o_bytes, kv_scale, (size_t)b * rows * (d / 32))))
         return SA_ERR_INVALID_ARG;
+    // the family this call runs in needs no more than sa_sparse_attn_workspace_size returns
+    const size_t need = sa::routed_workspace_bytes(fam, b, s, h, d, rows, topk);
+    if (!workspace || workspace_bytes < need) return SA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return SA_ERR_INVALID_ARG;
+    if (overlaps(o, o_bytes, workspace, need)) return SA_ERR_INVALID_ARG;
 
     sa::AttnCall c;
     c.q = q;
@@ -144,9 +174,7 @@ sa_status attn_call(const void* q, const void* kv, const uint8_t* kv_scale, int 
     c.rope = rope;
     c.rope_dim = rope_dim;
     c.rope_pos0 = rope_pos0;
-    if (rope) return from_cuda(sa::attn_tc_launch(c));  // the caller checked the tc family applies
-    if (sa::attn_tc_supports(h, d, kv_format, b, rows) && !force_mma())
-        return from_cuda(sa::attn_tc_launch(c));
+    if (fam == SA_FAMILY_TCGEN05) return from_cuda(sa::attn_tc_launch(c));
     return from_cuda(sa::attn_mma_launch(c));
 }
 

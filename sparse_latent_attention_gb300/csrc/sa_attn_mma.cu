@@ -27,7 +27,6 @@ constexpr int kHeadsPerCta = 64;
 constexpr int kTN = 64;            // gathered rows per tile
 constexpr int kPad = 8;            // bf16 padding per smem row: conflict-free ldmatrix
 constexpr int kThreads = 256;      // 4 head groups x 2 d-halves
-constexpr int kTargetCtas = 2 * 152;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Params {
@@ -409,11 +408,15 @@ struct Geometry {
     int n_tiles, n_splits, tiles_per_split, hblocks;
 };
 
-Geometry geometry(int64_t n_tokens, int h, int topk) {
+// The idx columns of a token are split over several CTAs when the tokens alone would not give
+// two CTAs per SM.  The split count grows with the SM count, so a workspace sized for
+// kMaxSmCount SMs covers every device.
+Geometry geometry(int64_t n_tokens, int h, int topk, int sms) {
     Geometry g;
     g.n_tiles = (topk + kTN - 1) / kTN;
     g.hblocks = (h + kHeadsPerCta - 1) / kHeadsPerCta;
     const int64_t base = n_tokens * g.hblocks;
+    const int64_t kTargetCtas = 2 * (int64_t)sms;
     int splits = 1;
     if (g.n_tiles > 1 && base < kTargetCtas) {
         splits = (int)((kTargetCtas + base - 1) / base);
@@ -463,7 +466,7 @@ cudaError_t launch_d(const AttnCall& c, const Params& p, dim3 grid) {
 }  // namespace
 
 size_t attn_mma_scratch_bytes(int64_t b, int64_t s, int h, int d, int topk) {
-    const Geometry g = geometry(b * s, h, topk);
+    const Geometry g = geometry(b * s, h, topk, kMaxSmCount);
     if (g.n_splits == 1) return 0;
     const size_t ntok = (size_t)(b * s);
     const size_t ml = align_up(ntok * g.n_splits * h * 2 * sizeof(float), 256);
@@ -473,7 +476,7 @@ size_t attn_mma_scratch_bytes(int64_t b, int64_t s, int h, int d, int topk) {
 
 cudaError_t attn_mma_launch(const AttnCall& c) {
     const int64_t n_tokens = c.b * c.s;
-    const Geometry g = geometry(n_tokens, c.h, c.topk);
+    const Geometry g = geometry(n_tokens, c.h, c.topk, device_sm_count());
     Params p;
     p.q = reinterpret_cast<const __nv_bfloat16*>(c.q);
     p.kv = c.kv;

@@ -140,11 +140,24 @@ __global__ void window_write_kernel(const __nv_bfloat16* x, int64_t nbatch, int6
 int grid_for(int64_t work, int per_block) {
     int64_t g = (work + per_block - 1) / per_block;
     if (g < 1) g = 1;
-    if (g > 152 * 32) g = 152 * 32;
+    const int64_t cap = (int64_t)device_sm_count() * 32;  // grid-stride loops beyond this
+    if (g > cap) g = cap;
     return (int)g;
 }
 
 }  // namespace
+
+int device_sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && counts[dev]) return counts[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    if (n > kMaxSmCount) n = kMaxSmCount;
+    if (dev >= 0 && dev < 64) counts[dev] = n;
+    return n;
+}
 
 cudaError_t window_idxs_launch(int64_t start_pos, int64_t seqlen, int window, int32_t* idx,
                                int64_t ld, int64_t nbatch, int64_t batch_stride,

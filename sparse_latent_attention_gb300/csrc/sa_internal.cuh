@@ -9,6 +9,13 @@
 
 namespace sa {
 
+// The kernels size their grids from the device's SM count, taken at most this large; workspace
+// sizes assume this many SMs, so that they depend on the shape only (GB300: 152).
+constexpr int kMaxSmCount = 160;
+
+// SMs of the current device, at most kMaxSmCount (cached per device; sa_helpers.cu).
+int device_sm_count();
+
 // Status word bits (first 32-bit word of the workspace status block).
 constexpr uint32_t kStatusBadIndex = 1u;
 constexpr uint32_t kStatusTimeout = 2u;
@@ -69,5 +76,11 @@ cudaError_t act_quant_launch(const void* x, int64_t n, int d, int64_t x_stride, 
                              uint8_t* scales, int64_t scales_stride, cudaStream_t stream);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Routing (sa_api.cu): the family a call runs in (SA_FAMILY_AUTO resolved; -1 = that family
+// cannot run the shape), and the workspace bytes that family needs for the shape.
+int routed_family(int family, int h, int d, int kv_format, int64_t b, int64_t rows);
+size_t routed_workspace_bytes(int family, int64_t b, int64_t s, int h, int d, int64_t rows,
+                              int topk);
 
 }  // namespace sa

@@ -20,6 +20,7 @@
 
 #include <mutex>
 
+#include "sa_internal.cuh"
 #include "sparse_attn.h"
 
 namespace {
@@ -63,18 +64,26 @@ extern "C" sa_status sa_sparse_attn_static_scratch(
     int topk, void* o, uint32_t* status_out, void* stream) {
     if (kv_format != SA_KV_BF16 && kv_format != SA_KV_FP8_E4M3) return SA_ERR_INVALID_ARG;
     if (b < 0 || s < 0 || h < 1 || d < 1 || rows < 0 || topk < 0) return SA_ERR_INVALID_ARG;
-    const size_t need = sa_sparse_attn_workspace_size(b, s, h, d, rows, topk, kv_format);
-    if (need == 0) return SA_ERR_UNSUPPORTED;
+    if (sa_sparse_attn_workspace_size(b, s, h, d, rows, topk, kv_format) == 0) return SA_ERR_UNSUPPORTED;
+    // the scratch of the family sa_sparse_attn routes this call to
+    const int fam = sa::routed_family(SA_FAMILY_AUTO, h, d, kv_format, b, rows);
+    if (fam < 0) return SA_ERR_UNSUPPORTED;
+    const size_t need = sa::routed_workspace_bytes(fam, b, s, h, d, rows, topk);
     if (need > (size_t)SA_STATIC_SCRATCH_BYTES) return SA_ERR_WORKSPACE;  // beyond the array
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     // sa_sparse_attn checks every other argument before it looks at the workspace, so a call
     // without one validates the arguments and enqueues nothing
     const sa_status pre = sa_sparse_attn(q, kv, kv_scale, kv_format, sink, idx, softmax_scale, b, s,
                                          h, d, rows, topk, o, nullptr, 0, stream);
-    if (pre != SA_ERR_WORKSPACE) return pre;  // an argument error, or SA_OK for b * s == 0
+    if (pre == SA_OK) {  // b * s == 0: nothing to compute, but the status word is still reported
+        if (status_out && cudaMemsetAsync(status_out, 0, sizeof(uint32_t), cs) != cudaSuccess)
+            return SA_ERR_CUDA;
+        return SA_OK;
+    }
+    if (pre != SA_ERR_WORKSPACE) return pre;  // an argument error
     void* scratch = nullptr;
     const sa_status st = scratch_address(&scratch);
     if (st != SA_OK) return st;
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(scratch, 0, SA_STATUS_BYTES, cs) != cudaSuccess) return SA_ERR_CUDA;
     const sa_status run = sa_sparse_attn(q, kv, kv_scale, kv_format, sink, idx, softmax_scale, b,
                                          s, h, d, rows, topk, o, scratch,

@@ -59,3 +59,20 @@ def test_roofline_line_binding_and_context():
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["traffic"] is None
     assert abs(r["frac"] - tfs / 1900.0) < 1e-4 and r["peak_source"] == "fallback (burst)"
     assert abs(r["context"]["tensor_frac_of_sustained"] - tfs / 1700.0) < 1e-4
+
+
+def test_both_arms_print_the_same_config():
+    from sparse_latent_attention_gb300 import workloads
+    wl = workloads.make_named("tiny")
+    a, b = bench.config_of(wl, 1), bench.config_of(wl, 1)
+    assert a == b and a["workload"] == "tiny" and "tokens_per_step" not in a
+    assert bench.DEFAULT_WORKLOAD == "cmp_prefill"
+    assert set(bench.TIMED_WORKLOADS) == {"swa_prefill", "cmp_prefill", "decode", "fp8_decode"}
+
+
+def test_e2e_link_floor():
+    link = {"h2d_gbs": 50.0, "d2h_gbs": 40.0, "duplex_gbs": 60.0}
+    # each direction alone: 1 GB in 20 ms, 0.4 GB out in 10 ms; together 1.4 GB at 60 GB/s
+    t = bench.e2e_link_floor_ms(link, 1e9, 4e8)
+    assert abs(t - 1.4e9 / 60e9 * 1e3) < 1e-9
+    assert abs(bench.e2e_link_floor_ms(link, 1e9, 0) - 20.0) < 1e-9

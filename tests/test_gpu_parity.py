@@ -28,7 +28,10 @@ def dev():
     return torch.device("cuda:0")
 
 
-def _sample_tokens(wl, n, seed=0):
+def _sample_tokens(wl, n, seed=0, runs=False):
+    """n sampled query tokens (all of them when n >= the workload's); with runs, also three whole
+    runs of 64 consecutive tokens -- at the start, the middle and the end -- so that every
+    position of a CTA's token sequence (and the row reuse between consecutive tokens) is met."""
     nt = wl.n_tokens
     if nt <= n:
         return np.arange(nt)
@@ -36,7 +39,11 @@ def _sample_tokens(wl, n, seed=0):
     fixed = np.array([0, 1, 2, 63, 64, 127, 128, 129, nt // 2, nt - 2, nt - 1])
     fixed = fixed[fixed < nt]
     rest = rng.choice(nt, size=n - len(fixed), replace=False)
-    return np.unique(np.concatenate([fixed, rest]))
+    parts = [fixed, rest]
+    if runs:
+        mid = nt // 2 - 32
+        parts += [np.arange(0, 64), np.arange(mid, mid + 64), np.arange(nt - 64, nt)]
+    return np.unique(np.concatenate(parts))
 
 
 def _oracle_on_tokens(wl, tokens, quantise):
@@ -189,7 +196,7 @@ def test_window_write_bit_exact(dev, nb, seqlen, start_pos, window, rows):
 # --------------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name,n_sample", [("tiny", 16), ("swa_prefill", 64), ("cmp_prefill", 48),
-                                           ("decode", 64), ("fp8_decode", 24)])
+                                           ("decode", 64), ("fp8_decode", 256)])
 def test_named_workload_parity(dev, name, n_sample):
     wl = workloads.make_named(name)
     quantise = name != "tiny"
@@ -198,7 +205,7 @@ def test_named_workload_parity(dev, name, n_sample):
     # the whole index table matches the oracle's composition bit for bit
     idx_want = compose_idx_oracle(wl)
     assert (x["idx"].cpu().numpy() == idx_want).all()
-    tokens = _sample_tokens(wl, n_sample)
+    tokens = _sample_tokens(wl, n_sample, runs=wl.s > 1)
     want, _ = _oracle_on_tokens(wl, tokens, quantise)
     got = _gpu.bf16_tensor_to_u16(o.view(wl.n_tokens, wl.h, wl.d)[torch.from_numpy(tokens).to(dev)])
     assert_close_bf16(got, want, ATOL, RTOL, what=name)
@@ -239,19 +246,30 @@ RANDOM_CASES = [
     (2, 9, 100, 512, 300, 200, {}),                 # 64 + 36 heads, two tiles
     (1, 12, 8, 512, 200, 130, {}),                  # fewer heads than one 32-row store box
     (3, 1, 40, 512, 2000, 600, {}),                 # decode split with a partial head block
+    # repeated indices in the tcgen05 family: ring placement falls back to column order, and a
+    # row kept from the previous pair may be listed twice
+    (1, 13, 64, 512, 64, 64, dict(distinct=False)),
+    (2, 30, 64, 512, 90, 200, dict(distinct=False)),
+    (3, 1, 64, 512, 300, 1152, dict(distinct=False)),  # cut decode ranges, many repeats
+    # cut ranges: few tokens, many pairs, pieces merged in the kernel (ragged last pair)
+    (1, 1, 64, 512, 9000, 4100, {}),
+    (7, 1, 128, 512, 3000, 2176, {}),
+    (2, 2, 64, 512, 5000, 1900, {}),
 ]
 
 
 @pytest.mark.parametrize("case", RANDOM_CASES, ids=lambda c: f"b{c[0]}s{c[1]}h{c[2]}d{c[3]}k{c[5]}")
 def test_random_parity(dev, case):
     b, s, h, d, rows, topk, extra = case
-    wl = workloads.make_random(b, s, h, d, rows, topk, seed=1000 + b * 7 + s, all_neg_tokens=(1,),
-                               **extra)
+    empty = (1,) if b * s > 1 else ()
+    wl = workloads.make_random(b, s, h, d, rows, topk, seed=1000 + b * 7 + s,
+                               all_neg_tokens=empty, **extra)
     o, x, ws = _gpu_run(wl, dev, quantise=False)
     assert sa.read_status(ws) == 0
     want = oracle.sparse_attn(wl.q, wl.kv_raw_dense(), wl.sink, compose_idx_oracle(wl), wl.scale)
     assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what=str(case))
-    assert (_gpu.bf16_tensor_to_u16(o.view(-1, h, d)[1]) == 0).all()
+    if empty:
+        assert (_gpu.bf16_tensor_to_u16(o.view(-1, h, d)[1]) == 0).all()
 
 
 ROPE_CASES = [
@@ -298,6 +316,57 @@ def test_inverse_rope_fused(dev, case):
     assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what=str(case))
 
 
+GUARD_CASES = [
+    # b, s, h, rows, topk, kv fp8, rope dims, start_pos
+    (2, 9, 100, 300, 200, False, 0, 0),        # 64 + 36 heads: clipped store boxes
+    (1, 12, 8, 200, 130, False, 0, 0),         # fewer heads than one store box
+    (3, 1, 40, 2000, 600, False, 0, 0),        # decode pieces merged into a partial head block
+    (5, 1, 64, 3000, 1152, False, 0, 0),       # decode pieces, full head block
+    (2, 9, 64, 300, 200, False, 64, 5),        # fused rotation
+    (3, 1, 64, 3000, 1152, False, 64, 4000),   # fused rotation on merged pieces
+    (2, 9, 40, 300, 200, True, 0, 0),          # fp8 kv, partial head block
+    (4, 1, 128, 3000, 2176, True, 0, 0),       # fp8 kv, two head blocks, pieces
+]
+
+
+@pytest.mark.parametrize("case", GUARD_CASES, ids=lambda c: f"b{c[0]}s{c[1]}h{c[2]}k{c[4]}"
+                         f"{'f8' if c[5] else ''}{'r' if c[6] else ''}")
+def test_o_guard_zones(dev, case):
+    """o inside a larger buffer filled with a sentinel: nothing outside o is written (clipped TMA
+    store boxes, merged pieces, the rotation), and o matches the oracle."""
+    b, s, h, rows, topk, fp8, rd, start_pos = case
+    d = 512
+    wl = workloads.make_random(b, s, h, d, rows, topk, seed=6100 + h + topk,
+                               all_neg_tokens=(1,) if b * s > 1 else (),
+                               kv_format="fp8" if fp8 else "bf16")
+    x = _gpu.prepare(wl, dev, quantise=fp8)
+    n = b * s * h * d
+    pad = 64 * 1024  # elements on each side (a multiple of 8: o stays 16-byte aligned)
+    sentinel = torch.tensor(-12345.0, dtype=torch.bfloat16)
+    buf = torch.full((pad + n + pad,), float(sentinel), dtype=torch.bfloat16, device=dev)
+    o = buf[pad:pad + n].view(b, s, h, d)
+    rope = None
+    if rd:
+        rot = workloads.rope_table(start_pos + s + 1, rd, seed=rd + start_pos)
+        rope = (torch.from_numpy(rot).to(dev), start_pos)
+    ws = sa.new_workspace(b, s, h, d, wl.rows, wl.topk,
+                          sa.SA_KV_FP8_E4M3 if fp8 else sa.SA_KV_BF16, device=dev)
+    sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, kv_scale=x["kv_scale"],
+                   out=o, workspace=ws, rope=rope)
+    torch.cuda.synchronize()
+    assert sa.read_status(ws) == 0
+    sent = sentinel.view(torch.int16).item()
+    assert (buf[:pad].view(torch.int16) == sent).all(), "written before o"
+    assert (buf[pad + n:].view(torch.int16) == sent).all(), "written after o"
+    kv_o = quantised_kv_oracle(wl, fp8)[0]
+    want = oracle.sparse_attn(wl.q, kv_o, wl.sink, compose_idx_oracle(wl), wl.scale)
+    if rd:
+        want = oracle.rope(want.reshape(b * s * h, d), rot,
+                           np.repeat(np.tile(start_pos + np.arange(s), b), h), rd,
+                           True).reshape(b, s, h, d)
+    assert_close_bf16(_gpu.bf16_tensor_to_u16(o), want, ATOL, RTOL, what=f"guard {case}")
+
+
 def test_running_max_raised_every_tile(dev):
     # The logits grow by ~7 nats (> 2^8 in log2 units) from one block of 64 rows to the next, so
     # a token that lists the rows in order raises its running maximum (and rescales O) on every
@@ -329,21 +398,33 @@ def test_running_max_raised_every_tile(dev):
 
 def test_query_parts_match_the_whole_call(dev):
     # Attending the query tokens in parts (as the benchmark's end-to-end step does, each part its
-    # own call on the same kv) gives the whole call's output bit for bit: a token's result does
-    # not depend on which other tokens share the call.
-    wl = workloads.make_random(1, 1200, 64, 512, 1400, 200, seed=4242, window=128)
+    # own call on the same kv) gives the whole call's output: bit for bit for a part of many
+    # tokens (each CTA takes whole tokens), and within the tolerance for a part of few tokens,
+    # whose idx columns the kernel may cut between SMs and merge (a different f32 summation
+    # order).  The same call twice gives the same bits: the merge order is fixed.
+    wl = workloads.make_random(1, 2600, 64, 512, 2800, 200, seed=4242, window=128)
     x = _gpu.prepare(wl, dev, quantise=False)
-    ws = sa.new_workspace(1, 1200, 64, 512, 1400, 200, device=dev)
+    ws = sa.new_workspace(1, 2600, 64, 512, 2800, 200, device=dev)
     whole = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, workspace=ws)
     parts = torch.empty_like(whole)
-    for a, b in ((0, 256), (256, 512), (512, 1000), (1000, 1200)):
-        wp = sa.new_workspace(1, b - a, 64, 512, 1400, 200, device=dev)
+    bounds = ((0, 1300), (1300, 2600), (0, 256), (256, 512), (512, 1000), (1000, 1300))
+    for i, (a, b) in enumerate(bounds):
+        wp = sa.new_workspace(1, b - a, 64, 512, 2800, 200, device=dev)
         sa.sparse_attn(x["q"][:, a:b], x["kv"], x["sink"], x["idx"][:, a:b], wl.scale,
                        out=parts[:, a:b], workspace=wp)
         assert sa.read_status(wp) == 0
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        if i == 1:  # two parts of 1300 tokens, each whole tokens per CTA
+            assert torch.equal(whole.view(torch.int16), parts.view(torch.int16))
     assert sa.read_status(ws) == 0
-    assert torch.equal(whole.view(torch.int16), parts.view(torch.int16))
+    assert_close_bf16(_gpu.bf16_tensor_to_u16(parts), _gpu.bf16_tensor_to_u16(whole), ATOL, RTOL,
+                      what="parts")
+    want = oracle.sparse_attn(wl.q, wl.kv_raw_dense(), wl.sink, compose_idx_oracle(wl), wl.scale,
+                              tokens=np.arange(0, 1300, 7))
+    assert_close_bf16(_gpu.bf16_tensor_to_u16(parts[0, 0:1300:7]), want, ATOL, RTOL, what="parts")
+    for a, b in bounds[2:]:  # the few-token parts again: the same bits
+        again = sa.sparse_attn(x["q"][:, a:b], x["kv"], x["sink"], x["idx"][:, a:b], wl.scale)
+        assert torch.equal(again.view(torch.int16), parts[:, a:b].view(torch.int16))
 
 
 def test_sink_minus_inf_and_single_row(dev):
@@ -398,13 +479,9 @@ def test_out_of_range_index_is_flagged_and_ignored(dev):
 @pytest.mark.parametrize("b,s,h,topk,window", [(2, 9, 64, 300, 0), (4, 1, 128, 2176, 0),
                                                (3, 1, 64, 1152, 0), (1, 140, 64, 128, 128),
                                                (2, 70, 64, 200, 128), (2, 5, 40, 300, 0)])
-def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk, window, family, monkeypatch):
+def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk, window, family):
     """Attention over e4m3 codes + e8m0 scales gives the same bits as attention over the bf16
     round trip of the same rows (same kernel family, tiling and order)."""
-    if family == "mma":
-        monkeypatch.setenv("SA_FORCE_MMA", "1")
-    else:
-        monkeypatch.delenv("SA_FORCE_MMA", raising=False)
     wl = workloads.make_random(b, s, h, 512, 2500, topk, seed=300 + topk, kv_format="fp8",
                                window=window)
     raw = _gpu.device_kv_raw(wl, dev)
@@ -416,24 +493,22 @@ def test_fp8_storage_bit_identical_to_round_trip(dev, b, s, h, topk, window, fam
     q = _gpu.u16_to_bf16_tensor(wl.q, dev)
     sink = torch.from_numpy(wl.sink).to(dev)
     idx = _gpu.device_idx(wl, dev)
-    o_fp8 = sa.sparse_attn(q, codes, sink, idx, wl.scale, kv_scale=scales)
-    o_bf16 = sa.sparse_attn(q, rt, sink, idx, wl.scale)
+    o_fp8 = sa.sparse_attn(q, codes, sink, idx, wl.scale, kv_scale=scales, family=family)
+    o_bf16 = sa.sparse_attn(q, rt, sink, idx, wl.scale, family=family)
     assert torch.equal(o_fp8.view(torch.int16), o_bf16.view(torch.int16))
 
 
 @pytest.mark.parametrize("case", [(2, 37, 64, 300, 200), (3, 1, 64, 5000, 1152),
                                   (1, 9, 128, 700, 650), (2, 7, 64, 400, 130)],
                          ids=lambda c: f"b{c[0]}s{c[1]}h{c[2]}k{c[4]}")
-def test_kernel_families_agree(dev, case, monkeypatch):
+def test_kernel_families_agree(dev, case):
     """The tcgen05 kernel (head_dim 512, bf16 kv) and the mma.sync kernel on the same inputs."""
     b, s, h, rows, topk = case
     wl = workloads.make_random(b, s, h, 512, rows, topk, seed=500 + topk, all_neg_tokens=(0,),
                                q_scale=4.0)
     x = _gpu.prepare(wl, dev, quantise=False)
-    o_tc = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale)
-    monkeypatch.setenv("SA_FORCE_MMA", "1")
-    o_mma = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale)
-    monkeypatch.delenv("SA_FORCE_MMA")
+    o_tc = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, family="tcgen05")
+    o_mma = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, family="mma")
     torch.cuda.synchronize()
     assert_close_bf16(_gpu.bf16_tensor_to_u16(o_tc), _gpu.bf16_tensor_to_u16(o_mma), ATOL, RTOL,
                       what="tc vs mma")

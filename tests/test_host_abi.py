@@ -21,7 +21,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == {"sa_sparse_attn", "sa_sparse_attn_workspace_size", "sa_window_idxs",
                           "sa_act_quant_fp8", "sa_read_status", "sa_status_string", "sa_version",
                           "sa_sparse_attn_static_scratch", "sa_window_write",
-                          "sa_sparse_attn_rope", "sa_indexer_topk",
+                          "sa_sparse_attn_rope", "sa_sparse_attn_family", "sa_indexer_topk",
                           "sa_candidate_blocks", "sa_hc_split_sinkhorn"}
     for n in names:
         assert hasattr(lib, n), n
@@ -72,9 +72,32 @@ def _attn(lib, **kw):
     (dict(ws=None), _lib.SA_ERR_WORKSPACE),
     (dict(ws_bytes=16), _lib.SA_ERR_WORKSPACE),
     (dict(o=FAKE), _lib.SA_ERR_INVALID_ARG),            # output overlaps the inputs
+    (dict(o=FAKE, ws=None), _lib.SA_ERR_INVALID_ARG),   # ... checked before the workspace
 ])
 def test_sparse_attn_rejects_bad_arguments(lib, kw, code):
     assert _attn(lib, **kw) == code
+
+
+def _attn_family(lib, family, **kw):
+    a = dict(q=FAKE, kv=FAKE, kv_scale=None, fmt=0, sink=FAKE, idx=FAKE, scale=0.1, b=1, s=2,
+             h=64, d=512, rows=8, topk=4, o=ctypes.c_void_p((1 << 40) + (1 << 30)), ws=None,
+             ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.sa_sparse_attn_family(a["q"], a["kv"], a["kv_scale"], a["fmt"], a["sink"],
+                                     a["idx"], a["scale"], a["b"], a["s"], a["h"], a["d"],
+                                     a["rows"], a["topk"], a["o"], a["ws"], a["ws_bytes"], family,
+                                     a["stream"])
+
+
+def test_sparse_attn_family_routing(lib):
+    # a valid call without a workspace gets as far as the workspace check in every family that
+    # can run the shape
+    for fam in (_lib.SA_FAMILY_AUTO, _lib.SA_FAMILY_TCGEN05, _lib.SA_FAMILY_MMA_SYNC):
+        assert _attn_family(lib, fam) == _lib.SA_ERR_WORKSPACE
+    assert _attn_family(lib, _lib.SA_FAMILY_MMA_SYNC, d=256) == _lib.SA_ERR_WORKSPACE
+    assert _attn_family(lib, _lib.SA_FAMILY_TCGEN05, d=256) == _lib.SA_ERR_UNSUPPORTED
+    assert _attn_family(lib, 3) == _lib.SA_ERR_INVALID_ARG
+    assert _attn_family(lib, -1) == _lib.SA_ERR_INVALID_ARG
 
 
 def _attn_rope(lib, **kw):
@@ -104,11 +127,6 @@ def _attn_rope(lib, **kw):
 ])
 def test_sparse_attn_rope_rejects_bad_arguments(lib, kw, code):
     assert _attn_rope(lib, **kw) == code
-
-
-def test_sparse_attn_rope_unsupported_on_forced_mma(lib, monkeypatch):
-    monkeypatch.setenv("SA_FORCE_MMA", "1")
-    assert _attn_rope(lib) == _lib.SA_ERR_UNSUPPORTED
 
 
 def _topk(lib, **kw):
