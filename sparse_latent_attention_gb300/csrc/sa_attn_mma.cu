@@ -358,6 +358,9 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_ml,
                                     const float* __restrict__ part_o,
                                     const float* __restrict__ sink, __nv_bfloat16* __restrict__ o,
                                     int h, int d, int n_splits) {
+    // the attention kernel this launch depends on has completed and its partials are visible
+    // after this point (a no-op when launched without the dependency)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t th = blockIdx.x;  // token * h + head
     const int hh = (int)(th % h);
     const int64_t token = th / h;
@@ -512,9 +515,20 @@ cudaError_t attn_combine_launch(const float* part_ml, const float* part_o, const
                                 void* o, int64_t n_tokens, int h, int d, int n_splits,
                                 cudaStream_t stream) {
     if (n_tokens * h == 0) return cudaSuccess;
-    attn_combine_kernel<<<(unsigned)(n_tokens * h), d / 4, 0, stream>>>(
-        part_ml, part_o, sink, reinterpret_cast<__nv_bfloat16*>(o), h, d, n_splits);
-    return cudaGetLastError();
+    // a programmatic dependent of the attention kernel just queued on the stream: its blocks can
+    // be scheduled while that kernel drains, and wait (griddepcontrol.wait) for its partials
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(n_tokens * h));
+    cfg.blockDim = dim3((unsigned)(d / 4));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel, part_ml, part_o, sink,
+                              reinterpret_cast<__nv_bfloat16*>(o), h, d, n_splits);
 }
 
 }  // namespace sa

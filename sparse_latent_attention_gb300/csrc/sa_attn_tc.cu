@@ -69,7 +69,6 @@ constexpr int kWarpEpilogue = kWarpSoftmax + 4;     // first epilogue warp
 constexpr int kThreads = 32 * (kWarpEpilogue + 4);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kPrefetchPairs = 8;          // pairs of a cut range pulled into L2 at the start
 // TMEM columns: O^T chunks (4 x 64), the two S buffers (2 x 64)
 constexpr uint32_t kColO = 0, kColS = 256;
 
@@ -126,8 +125,8 @@ struct Params {
     const float* sink;
     const int32_t* idx;
     __nv_bfloat16* o;
-    float* part_ml;            // [2 * groups][hblocks][64 heads][2]: a cut token's (max, sum)
-    float* part_o;             // [2 * groups][hblocks][64 heads][512]: its unnormalised O
+    float* part_ml;
+    float* part_o;
     uint32_t* status;
     float scale_log2;
     int64_t s_len;
@@ -136,104 +135,58 @@ struct Params {
     int64_t rows;
     int topk;
     int n_tiles;
-    int ppt;                   // pairs of tiles per token (a pair never straddles two tasks)
-    int unit_pairs;            // pairs per scheduling unit: ppt (whole tokens) or 1 (pairs)
-    int64_t n_units;           // scheduling units over all tokens
-    int64_t groups;            // CTA groups (gridDim.x / hblocks)
-    int prefetch_pairs;        // pairs of a CTA's range pulled into L2 when it starts (0 = none)
+    int n_splits;
+    int tiles_per_split;  // even when the columns are split, so that pairs never straddle tasks
+    int64_t n_units;      // (token, split) units; each is one task per head block
     const float* rope;    // inverse rotation of o's last rope_dim dims, or nullptr (see AttnCall)
     int rope_dim;
     int64_t rope_pos0;
 };
 
-// A task is one piece of a query token for this CTA's head block: the token's tiles [t0, t1).
-// A whole token (t0 == 0, t1 == n_tiles) is written to o directly; a piece of a token cut by the
-// range boundaries writes partials to its slot, which a second kernel merges.
 struct Task {
     int64_t token, seq, pos;  // query token (flat), its sequence and position in it
-    int hb, t0, t1;
-    bool whole;
-    int slot;                 // partial slot (pieces only): 2 g for the range's first task, else 2 g + 1
+    int hb, split, t0, t1;
 };
 
-// Scheduling.  The CTAs of one group (blockIdx.x / hblocks, one CTA per head block) serve the
-// same range of (token, pair-of-tiles) positions at the same time, so every kv row a group
-// gathers is read from HBM once and from L2 by the group's other CTAs.  A group takes a
-// contiguous range [pb, pe) of the flat pair positions (token-major), so that consecutive query
-// tokens of one sequence (which share most window rows) run back to back on the same SM.  With
-// many tokens the ranges are cut at token boundaries; with few (decode) at pair boundaries, so
-// that every SM gets work and the ranges are even.
-struct Range {
-    int64_t pb, pe;           // pair positions [pb, pe)
-    int64_t first_token;      // token of pb
-    int64_t n_tasks;          // tokens touched
-};
-
-__device__ __forceinline__ void unit_span(int64_t n_units, int64_t groups, int64_t g, int64_t& ub,
-                                          int64_t& ue) {
-    const int64_t base = n_units / groups, rem = n_units % groups;
-    ub = g * base + (g < rem ? g : rem);
-    ue = ub + base + (g < rem ? 1 : 0);
+// A CTA serves one head block, blockIdx.x % hblocks; the CTAs of one group (blockIdx.x /
+// hblocks) serve the same (token, split) units at the same time, so every kv row a group gathers
+// is read from HBM once and from L2 by the group's other CTAs.  A group takes a contiguous block
+// of units [begin, end), so that consecutive query tokens of one sequence (which share most
+// window rows) run back to back on the same SM.
+__device__ __forceinline__ void task_range(const Params& p, int64_t& begin, int64_t& end) {
+    const int64_t g = gridDim.x / p.hblocks, i = blockIdx.x / p.hblocks;
+    const int64_t base = p.n_units / g, rem = p.n_units % g;
+    begin = i * base + (i < rem ? i : rem);
+    end = begin + base + (i < rem ? 1 : 0);
 }
 
-__device__ __forceinline__ Range range_of_group(const Params& p, int64_t g) {
-    int64_t ub, ue;
-    unit_span(p.n_units, p.groups, g, ub, ue);
-    Range r;
-    r.pb = ub * p.unit_pairs;
-    r.pe = ue * p.unit_pairs;
-    r.first_token = r.pb / p.ppt;
-    r.n_tasks = r.pe > r.pb ? (r.pe - 1) / p.ppt - r.first_token + 1 : 0;
-    return r;
-}
-
-// The group whose range holds pair position q.
-__device__ __forceinline__ int64_t group_of_pair(int64_t n_units, int64_t groups, int unit_pairs,
-                                                 int64_t q) {
-    const int64_t base = n_units / groups, rem = n_units % groups;
-    const int64_t u = q / unit_pairs;
-    const int64_t big = rem * (base + 1);
-    return u < big ? u / (base + 1) : rem + (u - big) / base;
-}
-
-// The partial slot that group g gave token `token` (2 g for the group's first task, else 2 g + 1).
-__device__ __forceinline__ int64_t slot_of(int64_t n_units, int64_t groups, int unit_pairs, int ppt,
-                                           int64_t g, int64_t token) {
-    int64_t ub, ue;
-    unit_span(n_units, groups, g, ub, ue);
-    return 2 * g + ((ub * unit_pairs) / ppt == token ? 0 : 1);
-}
-
-// The tiles of token t inside the range [pb, pe).
-__device__ __forceinline__ void task_tiles(const Params& p, const Range& r, Task& t) {
-    const int64_t q0 = t.token * p.ppt;
-    const int64_t a = r.pb > q0 ? r.pb - q0 : 0;
-    const int64_t e = r.pe - q0 < p.ppt ? r.pe - q0 : p.ppt;
-    t.t0 = (int)(2 * a);
-    t.t1 = (int)min((int64_t)p.n_tiles, 2 * e);
-    t.whole = t.t0 == 0 && t.t1 == p.n_tiles;
-    const int64_t g = blockIdx.x / p.hblocks;
-    t.slot = (int)(2 * g + (t.token == r.first_token ? 0 : 1));
-}
-
-__device__ __forceinline__ Task task_first(const Params& p, const Range& r) {
+// The task of unit tau (token tau / n_splits, split tau % n_splits) for this CTA's head block.
+__device__ __forceinline__ Task task_of(const Params& p, int64_t tau) {
     Task t;
+    t.split = (int)(tau % p.n_splits);
     t.hb = (int)(blockIdx.x % p.hblocks);
-    t.token = r.first_token;
+    t.token = tau / p.n_splits;
     t.seq = t.token / p.s_len;
     t.pos = t.token - t.seq * p.s_len;
-    task_tiles(p, r, t);
+    t.t0 = t.split * p.tiles_per_split;
+    t.t1 = min(p.n_tiles, t.t0 + p.tiles_per_split);
+    if (t.t1 < t.t0) t.t1 = t.t0;
     return t;
 }
 
-// The next task (the next token), without divisions.
-__device__ __forceinline__ void task_step(const Params& p, const Range& r, Task& t) {
-    ++t.token;
-    if (++t.pos == p.s_len) {
-        t.pos = 0;
-        ++t.seq;
+// The task of the next unit (splits fastest, then tokens), without divisions.
+__device__ __forceinline__ void task_step(const Params& p, Task& t) {
+    if (++t.split == p.n_splits) {
+        t.split = 0;
+        ++t.token;
+        if (++t.pos == p.s_len) {
+            t.pos = 0;
+            ++t.seq;
+        }
     }
-    task_tiles(p, r, t);
+    t.t0 = t.split * p.tiles_per_split;
+    t.t1 = min(p.n_tiles, t.t0 + p.tiles_per_split);
+    if (t.t1 < t.t0) t.t1 = t.t0;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -384,11 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = M.tmem_base;
-    // a launch that depends on this one (the merge of cut tokens) may be scheduled from now on;
-    // it waits for this grid's completion before it reads anything
-    if (p.part_ml != nullptr && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const Range rg = range_of_group(p, blockIdx.x / p.hblocks);
-    const int64_t n_tasks = rg.n_tasks;
+    // a launch that depends on this one (the merge of split partials) may be scheduled from now
+    // on; it waits for this grid's completion before it reads anything
+    if (p.n_splits > 1 && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    int64_t tb, te;
+    task_range(p, tb, te);
 
     if (warp == 0) {
         // ------------------------------------------------------------------ MMA issue
@@ -430,7 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         if (p.n_tiles == 0) {
             // every task is empty (no idx columns): keep every phase in step
-            for (int64_t k = 0; k < n_tasks && ok; ++k) {
+            int64_t k = 0;
+            for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
                 const uint32_t kp = (uint32_t)(k & 1);
                 ok = warp_wait(smem_addr(&M.q_full), kp, abort);
                 mma_commit_elect(smem_addr(&M.q_empty));
@@ -445,33 +399,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             // one before.  Readiness is polled without blocking; the poll is bounded.
             struct Cursor {
                 Task t;
-                int64_t k;
+                int64_t tau, k;
                 int ti;
                 uint32_t T;
             };
             auto advance = [&](Cursor& c) {
                 ++c.T;
                 if (++c.ti == c.t.t1) {
+                    ++c.tau;
                     ++c.k;
-                    task_step(p, rg, c.t);
+                    task_step(p, c.t);
                     c.ti = c.t.t0;
                 }
             };
             Cursor cs;
-            cs.t = task_first(p, rg);
+            cs.t = task_of(p, tb);
+            cs.tau = tb;
             cs.k = 0;
             cs.ti = cs.t.t0;
             cs.T = 0;
             Cursor cv = cs;
             uint32_t idle = 0;
-            while (cv.k < n_tasks) {
+            while (cv.tau < te) {
                 bool did = false;
                 if (cv.T < cs.T &&
                     __all_sync(0xffffffffu, mbar_test_wait(smem_addr(&M.p_full[cv.T & 1]), (cv.T >> 1) & 1))) {
                     if (!(ok = issue_pv(cv.T, cv.ti == cv.t.t0, cv.ti == cv.t.t1 - 1, cv.k))) break;
                     advance(cv);
                     did = true;
-                } else if (cs.k < n_tasks) {
+                } else if (cs.tau < te) {
                     const uint32_t b = cs.T & 1, use = cs.T >> 1;
                     const bool first = cs.ti == cs.t.t0;
                     const bool rdy = mbar_test_wait(smem_addr(&M.s_empty[b]), (use & 1) ^ 1) &&
@@ -522,9 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int64_t k = 0;
             bool ok = true;
-            Task t = task_first(p, rg);
+            Task t = task_of(p, tb);
             const int hc = min(kHeads, p.h - hb * kHeads);
-            for (; k < n_tasks && ok; ++k, task_step(p, rg, t)) {
+            for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
                 const int32_t y = (int32_t)(t.token * p.h + (int64_t)t.hb * kHeads);
                 ok = mbar_wait(smem_addr(&M.q_empty), (uint32_t)(k & 1) ^ 1, abort);
                 if (!ok) break;
@@ -534,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 8; ++c)  // 8 boxes of [64 heads x 64 d], 128-byte swizzle
                     tma_load_2d(s_q + c * 8192, &q_map, 64 * c, y, bar);
                 // the next task's rows (when it is another token) into L2 meanwhile
-                if (k + 1 < n_tasks) {
+                if (tau + 1 < te && t.split == p.n_splits - 1) {
                     const __nv_bfloat16* qn = p.q + ((t.token + 1) * p.h + (int64_t)hb * kHeads) * kD;
 #pragma unroll 1
                     for (int i = 0; i < hc; i += 8)
@@ -556,14 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pt = (lane >> 4) * kRows + 16 * pw + (lane & 15);  // its pair column (and slot)
         uint32_t T = 0, pr_phase = 0, g3 = 0;
         bool ok = true;
-        Task t = task_first(p, rg);
-        for (int64_t k = 0; k < n_tasks && ok; ++k, task_step(p, rg, t)) {
+        Task t = task_of(p, tb);
+        for (int64_t tau = tb; tau < te && ok; ++tau, task_step(p, t)) {
             const int64_t bi = t.seq;
             const int32_t* idx_tok = p.idx + t.token * (int64_t)p.topk;
             const int colend = min(p.topk, t.t1 * kRows);
             for (int ti = t.t0; ti < t.t1 && ok; ti += 2) {
                 const int nt = min(2, t.t1 - ti);  // tiles of this pair
-                const int64_t pair_pos = t.token * p.ppt + (ti >> 1);  // in the flat pair order
                 const uint32_t gprev = g3 == 0 ? 2 : g3 - 1, gnext = g3 == 2 ? 0 : g3 + 1;
                 const int col = ti * kRows + pt;
                 int j = col < colend ? __ldg(idx_tok + col) : -1;
@@ -627,10 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t mh = half ? mh1 : mh0;
                     M.copy_list[pw][half][__popc(mh & ((1u << lane) - 1u))] = make_int2(j, ps);
                     // the buffers are usually still in use: pull the new rows into L2 now, so
-                    // that the copies issued once a buffer is released hit L2 (unless the pair
-                    // was among those pulled in when the CTA started)
-                    if (pair_pos < rg.pb + (int64_t)p.prefetch_pairs * p.hblocks) {
-                    } else if constexpr (kFp8) {
+                    // that the copies issued once a buffer is released hit L2
+                    if constexpr (kFp8) {
                         prefetch_l2(p.kv8 + (bi * p.rows + j) * (int64_t)kD, kD);
                         prefetch_l2(p.kv_scale + (bi * p.rows + j) * (int64_t)(kD / 32), kD / 32);
                     } else {
@@ -782,8 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t T = 0, sm_phase = 0, c3 = 0;
         int64_t k = 0;
         bool ok = true;
-        Task t = task_first(p, rg);
-        for (; k < n_tasks && ok; ++k, task_step(p, rg, t)) {
+        Task t = task_of(p, tb);
+        for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
             const int kpar = (int)(k & 1);
             float m = -INFINITY, mu = 0.f, l = 0.f;
             for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
@@ -889,55 +842,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int odd = lane & 1;
         const uint32_t sel = odd ? 0x3276u : 0x5410u;
         const uint32_t st_base = s_box + 4 * (lane >> 1) + 64 * odd;
-        const int et = tid - 32 * kWarpEpilogue;  // 0 .. 127
         int64_t k = 0;
         bool ok = true;
-        Task t = task_first(p, rg);
-        if (p.prefetch_pairs > 0) {
-            // A short range (decode): pull the rows of its first pairs into L2 while the pipeline
-            // starts, so that they stream from HBM at the full rate instead of a pair at a time
-            // behind the copies.  The idx entries are loaded together (one column of each pair
-            // per thread), then each row's 128-byte lines are prefetched by the load/store units
-            // (not the copy engine, which the Q loads and o stores use).  The CTAs of a group
-            // split the pairs between them.
-            int rowj[kPrefetchPairs];
-            int64_t rowb[kPrefetchPairs];
-#pragma unroll
-            for (int i = 0; i < kPrefetchPairs; ++i) {
-                const int64_t q = rg.pb + t.hb + (int64_t)i * p.hblocks;
-                rowj[i] = -1;
-                rowb[i] = 0;
-                if (i < p.prefetch_pairs && q < rg.pe) {
-                    const int64_t tok = q / p.ppt;
-                    const int col = (int)(q - tok * p.ppt) * (2 * kRows) + et;
-                    rowb[i] = (tok / p.s_len) * p.rows;
-                    if (col < p.topk) rowj[i] = __ldg(p.idx + tok * (int64_t)p.topk + col);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kPrefetchPairs; ++i) {
-                const int j = rowj[i];
-                if (j < 0 || j >= p.rows) continue;
-                const int64_t rowi = rowb[i] + j;
-                if constexpr (kFp8) {
-                    const uint8_t* r8 = p.kv8 + rowi * kD;
-#pragma unroll
-                    for (int l = 0; l < kD / 128; ++l) prefetch_line_l2(r8 + 128 * l);
-                    prefetch_line_l2(p.kv_scale + rowi * (kD / 32));
-                } else {
-                    const uint8_t* r16 = reinterpret_cast<const uint8_t*>(p.kv + rowi * kD);
-#pragma unroll
-                    for (int l = 0; l < 2 * kD / 128; ++l) prefetch_line_l2(r16 + 128 * l);
-                }
-            }
-        }
+        Task t = task_of(p, tb);
         // fp8: the next tile whose chunks 2 and 3 this warpgroup widens (warp q4 takes the rows
         // producer warp q4 listed)
-        Task wt = t;
-        int64_t wk = 0;
-        int wti = t.t0;
+        int64_t wtau = p.n_tiles > 0 ? tb : te;
+        int wsplit = t.split, wt0 = t.t0, wt1 = t.t1, wti = t.t0;
         uint32_t wT = 0;
-        for (; k < n_tasks && ok; ++k, task_step(p, rg, t)) {
+        for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
             const int kpar = (int)(k & 1);
             const int h0 = t.hb * kHeads;
             const int hc = min(kHeads, p.h - h0);
@@ -955,9 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (its last tile needs this warpgroup's widening first); the poll is bounded
                 uint32_t idle = 0;
                 while (true) {
-                    if (wk < n_tasks &&
+                    if (wtau < te &&
                         __all_sync(0xffffffffu, mbar_test_wait(smem_addr(&M.staged[wT & 1]), (wT >> 1) & 1))) {
-                        const int hx = (wti - wt.t0) & 1;
+                        const int hx = (wti - wt0) & 1;
                         const int ncopy = M.copy_n[q4][hx];
                         int2 ent8[8];
 #pragma unroll
@@ -969,10 +882,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fence_proxy_async_smem();
                         mbar_arrive(smem_addr(&M.kv_full[wT & 1]));
                         ++wT;
-                        if (++wti == wt.t1) {  // the next task's tiles
-                            ++wk;
-                            task_step(p, rg, wt);
-                            wti = wt.t0;
+                        if (++wti == wt1) {  // the next unit's tiles (splits fastest, as task_step)
+                            ++wtau;
+                            if (++wsplit == p.n_splits) wsplit = 0;
+                            wt0 = wsplit * p.tiles_per_split;
+                            wt1 = min(p.n_tiles, wt0 + p.tiles_per_split);
+                            wti = wt0;
                         }
                         idle = 0;
                         continue;
@@ -989,8 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ok && mbar_wait(smem_addr(&M.o_full), (uint32_t)kpar, abort);
             if (ok) ok = mbar_wait(smem_addr(&M.stats_full[kpar]), (uint32_t)((k >> 1) & 1), abort);
             tc_fence_after();
-            const bool split = !t.whole;  // a piece of a cut token: partials to its slot
-            const int64_t pbase = ((int64_t)t.slot * p.hblocks + t.hb) * kHeads;
+            const bool split = p.n_splits > 1;
+            const int64_t pbase = (t.token * p.n_splits + t.split) * (int64_t)p.h + h0;
             // the denominators: lane l finishes heads l and l + 32 into the warp's own table
 #pragma unroll
             for (int hq = 0; hq < 2; ++hq) {
@@ -1094,80 +1009,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-struct CombineParams {
-    const float* part_ml;
-    const float* part_o;
-    const float* sink;
-    __nv_bfloat16* o;
-    int64_t n_units, groups;
-    int unit_pairs, ppt, h, hblocks;
-};
-
-// Merge of a cut token's pieces (the split-idx form of the page's sparse_attn, with the sink added
-// once): M = max over pieces of m; o = sum 2^(m - M) O / (2^(sink log2e - M) + sum 2^(m - M) l),
-// zero when no piece summed a row.  One block of 128 threads per (token, head); thread e merges
-// d = 4 e .. 4 e + 3, loading the statistics and columns of four pieces at a time.  A whole token
-// (one piece) was written by the attention kernel and is skipped.
-__global__ void __launch_bounds__(kD / 4) pieces_combine_kernel(const CombineParams c) {
-    const int64_t th = blockIdx.x;
-    const int hh = (int)(th % c.h);
-    const int64_t token = th / c.h;
-    const int64_t q0 = token * c.ppt;
-    const int64_t ga = group_of_pair(c.n_units, c.groups, c.unit_pairs, q0);
-    const int64_t gb = group_of_pair(c.n_units, c.groups, c.unit_pairs, q0 + c.ppt - 1);
-    if (ga == gb) return;
-    // the attention kernel (the launch this one depends on) has completed and its partials are
-    // visible after this point
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int hb = hh / kHeads, i = hh % kHeads;
-    const int e = threadIdx.x;
-    float M = -INFINITY, L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-    for (int64_t g0 = ga; g0 <= gb; g0 += 4) {
-        float2 ml[4];
-        float4 v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int64_t g = g0 + k;
-            ml[k] = make_float2(0.f, 0.f);
-            v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (g <= gb) {
-                const int64_t row =
-                    (slot_of(c.n_units, c.groups, c.unit_pairs, c.ppt, g, token) * c.hblocks + hb) *
-                        kHeads + i;
-                ml[k] = reinterpret_cast<const float2*>(c.part_ml)[row];
-                v[k] = reinterpret_cast<const float4*>(c.part_o + row * kD)[e];
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            if (!(ml[k].y > 0.f)) continue;  // the piece listed no row (or is past the last)
-            if (ml[k].x > M) {  // a new maximum: rescale what was summed so far (0 at the start)
-                const float r = M == -INFINITY ? 0.f : fast_exp2(M - ml[k].x);
-                L *= r;
-                acc.x *= r;
-                acc.y *= r;
-                acc.z *= r;
-                acc.w *= r;
-                M = ml[k].x;
-            }
-            const float w = fast_exp2(ml[k].x - M);
-            L += w * ml[k].y;
-            acc.x += w * v[k].x;
-            acc.y += w * v[k].y;
-            acc.z += w * v[k].z;
-            acc.w += w * v[k].w;
-        }
-    }
-    const float Mu = M == -INFINITY ? 0.f : M;
-    const float inv = L > 0.f ? 1.f / (L + fast_exp2(c.sink[hh] * kLog2e - Mu)) : 0.f;
-    uint2 out;
-    out.x = pack_bf16(acc.x * inv, acc.y * inv);
-    out.y = pack_bf16(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(c.o + th * (int64_t)kD + 4 * e) = out;
-}
-
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
@@ -1187,47 +1028,32 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 struct TcGeometry {
-    int n_tiles, hblocks, ppt, unit_pairs;
-    int64_t groups, n_units;
-    bool cut;  // ranges cut at pair boundaries (tokens may be split between groups)
+    int n_tiles, hblocks, n_splits, tiles_per_split;
 };
 
-// One persistent CTA per SM (and head block).  With many tokens per group the ranges hold whole
-// tokens; with fewer than kTokensPerGroupForWhole per group (decode) they are cut at pairs of
-// tiles, so that every SM gets an even share; the cut tokens are merged by a second kernel.
-constexpr int64_t kTokensPerGroupForWhole = 8;
-
+// Split the idx columns of a token over several tasks only when the tokens alone cannot fill
+// the GPU's SMs (decode), at pair-of-tiles boundaries.  The split count grows with the SM count,
+// so a workspace sized for kMaxSmCount SMs covers every device.
 TcGeometry tc_geometry(int64_t n_tokens, int h, int topk, int sms) {
     TcGeometry g;
     g.n_tiles = (topk + kRows - 1) / kRows;
     g.hblocks = (h + kHeads - 1) / kHeads;
-    g.ppt = (g.n_tiles + 1) / 2;
-    int64_t groups = sms / g.hblocks;
-    if (groups < 1) groups = 1;
-    g.cut = g.ppt > 1 && n_tokens < kTokensPerGroupForWhole * groups;
-    g.unit_pairs = g.cut ? 1 : g.ppt;
-    g.n_units = g.cut ? n_tokens * g.ppt : n_tokens;
-    g.groups = groups < g.n_units ? groups : g.n_units;
-    if (g.groups < 1) g.groups = 1;
+    const int pairs = (g.n_tiles + 1) / 2;
+    const int64_t base = n_tokens * g.hblocks;
+    int splits = 1;
+    if (pairs > 1 && base < sms) {
+        splits = (int)(sms / base);
+        if (splits > pairs) splits = pairs;
+        if (splits < 1) splits = 1;
+    }
+    if (splits > 1) {
+        g.tiles_per_split = 2 * ((pairs + splits - 1) / splits);
+        g.n_splits = (g.n_tiles + g.tiles_per_split - 1) / g.tiles_per_split;
+    } else {
+        g.tiles_per_split = g.n_tiles > 0 ? g.n_tiles : 1;
+        g.n_splits = 1;
+    }
     return g;
-}
-
-struct TcScratch {
-    size_t ml, o;  // byte offsets inside the scratch
-    size_t bytes;
-};
-
-// Scratch of a cut-range launch, sized for the largest device (kMaxSmCount SMs), so that it is
-// a function of the shape only: 2 partial slots per group.
-TcScratch tc_scratch(int64_t n_tokens, int h, int topk) {
-    TcScratch sc{0, 0, 0};
-    const TcGeometry g = tc_geometry(n_tokens, h, topk, kMaxSmCount);
-    if (!g.cut) return sc;
-    const size_t slots = 2 * (size_t)g.groups * g.hblocks * kHeads;
-    sc.ml = 0;
-    sc.o = align_up(slots * 2 * sizeof(float), 256);
-    sc.bytes = sc.o + slots * kD * sizeof(float);
-    return sc;
 }
 
 }  // namespace
@@ -1240,7 +1066,11 @@ bool attn_tc_supports(int h, int d, int kv_format, int64_t b, int64_t rows) {
 }
 
 size_t attn_tc_scratch_bytes(int64_t b, int64_t s, int h, int topk) {
-    return tc_scratch(b * s, h, topk).bytes;
+    const TcGeometry g = tc_geometry(b * s, h, topk, kMaxSmCount);
+    if (g.n_splits == 1) return 0;
+    const size_t ntok = (size_t)(b * s);
+    const size_t ml = align_up(ntok * g.n_splits * h * 2 * sizeof(float), 256);
+    return ml + ntok * g.n_splits * h * (size_t)kD * sizeof(float);
 }
 
 cudaError_t attn_tc_launch(const AttnCall& c) {
@@ -1291,19 +1121,15 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
     p.rows = c.rows;
     p.topk = c.topk;
     p.n_tiles = g.n_tiles;
-    p.ppt = g.ppt;
-    p.unit_pairs = g.unit_pairs;
-    p.n_units = g.n_units;
-    p.prefetch_pairs = g.cut ? kPrefetchPairs : 0;
-    p.groups = g.groups;
+    p.n_splits = g.n_splits;
+    p.tiles_per_split = g.tiles_per_split;
+    p.n_units = n_tokens * g.n_splits;
     p.part_ml = nullptr;
     p.part_o = nullptr;
-    if (g.cut) {
-        const TcScratch sc = tc_scratch(n_tokens, c.h, c.topk);
-        if (c.scratch_bytes < sc.bytes) return cudaErrorInvalidValue;  // the caller checked the size
-        uint8_t* base = reinterpret_cast<uint8_t*>(c.scratch);
-        p.part_ml = reinterpret_cast<float*>(base + sc.ml);
-        p.part_o = reinterpret_cast<float*>(base + sc.o);
+    if (g.n_splits > 1) {
+        const size_t ml = align_up((size_t)n_tokens * g.n_splits * c.h * 2 * sizeof(float), 256);
+        p.part_ml = reinterpret_cast<float*>(c.scratch);
+        p.part_o = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(c.scratch) + ml);
     }
 
     static bool configured[64] = {};
@@ -1321,38 +1147,18 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
         }
         if (dev < 64) configured[dev] = true;
     }
-    const int64_t grid = g.groups * g.hblocks;  // CTA groups, one CTA per head block
+    int64_t groups = device_sm_count() / g.hblocks;  // CTA groups, one CTA per head block
+    if (groups > p.n_units) groups = p.n_units;
+    if (groups < 1) groups = 1;
+    const int64_t grid = groups * g.hblocks;
     const bool rope = c.rope != nullptr;
     auto kernel = fp8 ? (rope ? attn_tc_kernel<true, true> : attn_tc_kernel<true, false>)
                       : (rope ? attn_tc_kernel<false, true> : attn_tc_kernel<false, false>);
     kernel<<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
     e = cudaGetLastError();
-    if (e != cudaSuccess || !g.cut) return e;
-    // the merge of the cut tokens, launched as a programmatic dependent of the attention kernel:
-    // its blocks are scheduled while the attention kernel drains and wait (griddepcontrol.wait)
-    // for its partials
-    CombineParams cp;
-    cp.part_ml = p.part_ml;
-    cp.part_o = p.part_o;
-    cp.sink = c.sink;
-    cp.o = p.o;
-    cp.n_units = g.n_units;
-    cp.groups = g.groups;
-    cp.unit_pairs = g.unit_pairs;
-    cp.ppt = g.ppt;
-    cp.h = c.h;
-    cp.hblocks = g.hblocks;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(n_tokens * c.h));
-    cfg.blockDim = dim3(kD / 4);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, pieces_combine_kernel, cp);
+    if (e != cudaSuccess || g.n_splits == 1) return e;
+    return attn_combine_launch(p.part_ml, p.part_o, c.sink, c.o, n_tokens, c.h, kD, g.n_splits,
+                               c.stream);
 }
 
 }  // namespace sa
