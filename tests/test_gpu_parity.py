@@ -125,6 +125,26 @@ def test_act_quant_bit_exact(dev):
     assert (cscale[:, 1].cpu().numpy() == want_sc).all()
 
 
+def test_act_quant_both_kernel_shapes(dev):
+    """Rows whose strides allow 16-byte accesses take the eight-per-thread kernel; others (an odd
+    row stride, a misaligned start) the one-element-per-lane kernel: both bit-exact."""
+    bits = _act_quant_inputs()[:96, :256]
+    want_rt, want_codes, want_sc = oracle.act_quant(bits)
+    for stride, offset in ((256, 0), (264, 8), (259, 0), (256, 1)):
+        buf = torch.zeros(96 * stride + offset + 8, dtype=torch.bfloat16, device=dev)
+        x = buf[offset:offset + 96 * stride].view(96, stride)[:, :256]
+        x.copy_(_gpu.u16_to_bf16_tensor(bits, dev))
+        rt = torch.empty((96, 256), dtype=torch.bfloat16, device=dev)
+        codes = torch.empty((96, 256), dtype=torch.uint8, device=dev)
+        sc = torch.empty((96, 8), dtype=torch.uint8, device=dev)
+        sa.act_quant_fp8(x, out_rt=rt, codes=codes, scales=sc)
+        assert (_gpu.bf16_tensor_to_u16(rt) == want_rt).all(), (stride, offset)
+        assert (codes.cpu().numpy() == want_codes).all(), (stride, offset)
+        assert (sc.cpu().numpy() == want_sc).all(), (stride, offset)
+        sa.act_quant_fp8(x, out_rt=x)  # in place, strided
+        assert (_gpu.bf16_tensor_to_u16(x.contiguous()) == want_rt).all(), (stride, offset)
+
+
 def test_act_quant_every_bf16_value(dev):
     """Each of the 65536 bf16 patterns (NaN and inf excluded) inside a block with a fixed
     amax, so every e4m3 rounding case and both signs are met."""
