@@ -112,6 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(Params p) {
     __nv_bfloat16* sKV = sQ + kHeadsPerCta * LD;
     int* sRow = reinterpret_cast<int*>(sKV + 2 * kTN * LD);
 
+    // every global access of this kernel comes after the work queued before it on the stream
+    pdl_wait();
+    pdl_trigger();
     const int64_t token = blockIdx.x;
     const int split = blockIdx.y;
     const int h0 = blockIdx.z * kHeadsPerCta;
@@ -359,8 +362,9 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_ml,
                                     const float* __restrict__ sink, __nv_bfloat16* __restrict__ o,
                                     int h, int d, int n_splits) {
     // the attention kernel this launch depends on has completed and its partials are visible
-    // after this point (a no-op when launched without the dependency)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // after this point
+    pdl_wait();
+    pdl_trigger();
     const int64_t th = blockIdx.x;  // token * h + head
     const int hh = (int)(th % h);
     const int64_t token = th / h;
@@ -447,8 +451,7 @@ cudaError_t launch_t(const AttnCall& c, const Params& p, dim3 grid) {
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = true;
     }
-    attn_mma_kernel<D, kFp8><<<grid, kThreads, smem, c.stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(attn_mma_kernel<D, kFp8>, grid, dim3(kThreads), smem, c.stream, p);
 }
 
 template <bool kFp8>
@@ -516,19 +519,10 @@ cudaError_t attn_combine_launch(const float* part_ml, const float* part_o, const
                                 cudaStream_t stream) {
     if (n_tokens * h == 0) return cudaSuccess;
     // a programmatic dependent of the attention kernel just queued on the stream: its blocks can
-    // be scheduled while that kernel drains, and wait (griddepcontrol.wait) for its partials
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(n_tokens * h));
-    cfg.blockDim = dim3((unsigned)(d / 4));
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_combine_kernel, part_ml, part_o, sink,
-                              reinterpret_cast<__nv_bfloat16*>(o), h, d, n_splits);
+    // be scheduled while that kernel drains, and wait for its partials
+    return launch_pdl(attn_combine_kernel, dim3((unsigned)(n_tokens * h)), dim3((unsigned)(d / 4)), 0,
+                      stream, part_ml, part_o, sink, reinterpret_cast<__nv_bfloat16*>(o), h, d,
+                      n_splits);
 }
 
 }  // namespace sa

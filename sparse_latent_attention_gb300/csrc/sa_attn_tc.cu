@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &M.abort;
     const int hb = (int)(blockIdx.x % p.hblocks);
+    pdl_trigger();  // the next launch on the stream may be scheduled from now on
 
     if (tid == 0) {
         mbar_init(smem_addr(&M.q_full), 1);
@@ -326,20 +327,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         M.pair_seq[tid] = -1;
         M.need_corr[tid] = 0;
     }
-    for (int i = tid; i < kHeads; i += kThreads)
-        M.sink[i] = hb * kHeads + i < p.h ? p.sink[hb * kHeads + i] : 0.f;
     for (uint32_t i = tid; i < kKvBytes / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + kOffKv)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1 && lane == 0) tma_prefetch_desc(&q_map);
     if (warp == kWarpEpilogue && lane == 0) tma_prefetch_desc(&o_map);
+    // the set-up above touches no global memory; everything below may read what the work queued
+    // before this launch writes
+    pdl_wait();
+    for (int i = tid; i < kHeads; i += kThreads)
+        M.sink[i] = hb * kHeads + i < p.h ? p.sink[hb * kHeads + i] : 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = M.tmem_base;
-    // a launch that depends on this one (the merge of split partials) may be scheduled from now
-    // on; it waits for this grid's completion before it reads anything
-    if (p.n_splits > 1 && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int64_t tb, te;
     task_range(p, tb, te);
 
@@ -1154,8 +1155,7 @@ cudaError_t attn_tc_launch(const AttnCall& c) {
     const bool rope = c.rope != nullptr;
     auto kernel = fp8 ? (rope ? attn_tc_kernel<true, true> : attn_tc_kernel<true, false>)
                       : (rope ? attn_tc_kernel<false, true> : attn_tc_kernel<false, false>);
-    kernel<<<(unsigned)grid, kThreads, kSmemBytes, c.stream>>>(qmap, omap, p);
-    e = cudaGetLastError();
+    e = launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, c.stream, qmap, omap, p);
     if (e != cudaSuccess || g.n_splits == 1) return e;
     return attn_combine_launch(p.part_ml, p.part_o, c.sink, c.o, n_tokens, c.h, kD, g.n_splits,
                                c.stream);

@@ -22,6 +22,8 @@ namespace {
 // ring read oldest first, column j holds the slot of position p - window + 1 + j.
 __global__ void window_idxs_kernel(int64_t start_pos, int64_t seqlen, int window, int32_t* idx,
                                    int64_t ld, int64_t nbatch, int64_t batch_stride) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t per_batch = seqlen * window;
     const int64_t total = per_batch * nbatch;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
@@ -46,6 +48,8 @@ __global__ void window_idxs_kernel(int64_t start_pos, int64_t seqlen, int window
 // idx 16-byte aligned, fewer than 2^31 groups of four): 32-bit index arithmetic only.
 __global__ void window_idxs4_kernel(int64_t start_pos, int seqlen, int window, int32_t* idx,
                                     int64_t ld, int nbatch, int64_t batch_stride) {
+    pdl_wait();
+    pdl_trigger();
     const int w4 = window >> 2;
     const int per_batch = seqlen * w4;
     const int total = per_batch * nbatch;
@@ -116,6 +120,8 @@ __global__ void act_quant_kernel(const __nv_bfloat16* x, int64_t n, int d,
                                  int64_t xs, __nv_bfloat16* x_rt, int64_t rts,
                                  uint8_t* __restrict__ codes, int64_t cs,
                                  uint8_t* __restrict__ scales, int64_t ss) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int blocks_per_row = d / 32;
     const int64_t total = n * blocks_per_row;
@@ -140,6 +146,8 @@ __global__ void window_write_kernel(const __nv_bfloat16* x, int64_t nbatch, int6
                                     __nv_bfloat16* rt, int64_t rts, int64_t rtb,
                                     uint8_t* __restrict__ codes, int64_t cs, int64_t cbs,
                                     uint8_t* __restrict__ scales, int64_t ss, int64_t sbs) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int blocks_per_row = d / 32;
     const int64_t t_first = seqlen > window ? seqlen - window : 0;
@@ -211,6 +219,8 @@ __device__ __forceinline__ void quant_group8(uint4 in, __nv_bfloat16* rt, uint8_
 __global__ void act_quant8_kernel(const __nv_bfloat16* x, int64_t n, int d, int64_t xs,
                                   __nv_bfloat16* x_rt, int64_t rts, uint8_t* codes, int64_t cs,
                                   uint8_t* scales, int64_t ss) {
+    pdl_wait();
+    pdl_trigger();
     const int g8 = d >> 3;
     const int total = (int)(n * g8);
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
@@ -230,6 +240,8 @@ __global__ void window_write8_kernel(const __nv_bfloat16* x, int64_t nbatch, int
                                      __nv_bfloat16* rt, int64_t rts, int64_t rtb,
                                      uint8_t* codes, int64_t cs, int64_t cbs,
                                      uint8_t* scales, int64_t ss, int64_t sbs) {
+    pdl_wait();
+    pdl_trigger();
     const int g8 = d >> 3;
     const int64_t t_first = seqlen > window ? seqlen - window : 0;
     const int per_seq = (int)(seqlen - t_first);
@@ -279,13 +291,11 @@ cudaError_t window_idxs_launch(int64_t start_pos, int64_t seqlen, int window, in
     if (total == 0) return cudaSuccess;
     if (window % 4 == 0 && ld % 4 == 0 && (nbatch == 1 || batch_stride % 4 == 0) && a16(idx) &&
         total / 4 < (int64_t(1) << 31) && seqlen < (int64_t(1) << 31)) {
-        window_idxs4_kernel<<<grid_for(total / 4, 256), 256, 0, stream>>>(
-            start_pos, (int)seqlen, window, idx, ld, (int)nbatch, batch_stride);
-        return cudaGetLastError();
+        return launch_pdl(window_idxs4_kernel, dim3(grid_for(total / 4, 256)), dim3(256), 0, stream,
+                          start_pos, (int)seqlen, window, idx, ld, (int)nbatch, batch_stride);
     }
-    window_idxs_kernel<<<grid_for(total, 256), 256, 0, stream>>>(start_pos, seqlen, window, idx,
-                                                                  ld, nbatch, batch_stride);
-    return cudaGetLastError();
+    return launch_pdl(window_idxs_kernel, dim3(grid_for(total, 256)), dim3(256), 0, stream,
+                      start_pos, seqlen, window, idx, ld, nbatch, batch_stride);
 }
 
 cudaError_t act_quant_launch(const void* x, int64_t n, int d, int64_t x_stride, void* x_rt,
@@ -295,15 +305,13 @@ cudaError_t act_quant_launch(const void* x, int64_t n, int d, int64_t x_stride, 
     if (total_threads == 0) return cudaSuccess;
     if (a16(x) && x_stride % 8 == 0 && (!x_rt || (a16(x_rt) && rt_stride % 8 == 0)) &&
         (!codes || (a8(codes) && codes_stride % 8 == 0)) && total_threads / 8 < (int64_t(1) << 31)) {
-        act_quant8_kernel<<<grid_for(total_threads / 8, 256), 256, 0, stream>>>(
-            (const __nv_bfloat16*)x, n, d, x_stride, (__nv_bfloat16*)x_rt, rt_stride, codes,
-            codes_stride, scales, scales_stride);
-        return cudaGetLastError();
+        return launch_pdl(act_quant8_kernel, dim3(grid_for(total_threads / 8, 256)), dim3(256), 0,
+                          stream, (const __nv_bfloat16*)x, n, d, x_stride, (__nv_bfloat16*)x_rt,
+                          rt_stride, codes, codes_stride, scales, scales_stride);
     }
-    act_quant_kernel<<<grid_for(total_threads, 256), 256, 0, stream>>>(
-        (const __nv_bfloat16*)x, n, d, x_stride, (__nv_bfloat16*)x_rt, rt_stride, codes,
-        codes_stride, scales, scales_stride);
-    return cudaGetLastError();
+    return launch_pdl(act_quant_kernel, dim3(grid_for(total_threads, 256)), dim3(256), 0, stream,
+                      (const __nv_bfloat16*)x, n, d, x_stride, (__nv_bfloat16*)x_rt, rt_stride,
+                      codes, codes_stride, scales, scales_stride);
 }
 
 cudaError_t window_write_launch(const void* x, int64_t nbatch, int64_t seqlen, int d,
@@ -318,17 +326,16 @@ cudaError_t window_write_launch(const void* x, int64_t nbatch, int64_t seqlen, i
         (!ring_rt || (a16(ring_rt) && rt_stride % 8 == 0 && rt_batch_stride % 8 == 0)) &&
         (!codes || (a8(codes) && codes_stride % 8 == 0 && codes_batch_stride % 8 == 0)) &&
         rows * d / 8 < (int64_t(1) << 31)) {
-        window_write8_kernel<<<grid_for(rows * d / 8, 256), 256, 0, stream>>>(
-            (const __nv_bfloat16*)x, nbatch, seqlen, d, x_stride, start_pos, window,
-            (__nv_bfloat16*)ring_rt, rt_stride, rt_batch_stride, codes, codes_stride,
-            codes_batch_stride, scales, scales_stride, scales_batch_stride);
-        return cudaGetLastError();
+        return launch_pdl(window_write8_kernel, dim3(grid_for(rows * d / 8, 256)), dim3(256), 0,
+                          stream, (const __nv_bfloat16*)x, nbatch, seqlen, d, x_stride, start_pos,
+                          window, (__nv_bfloat16*)ring_rt, rt_stride, rt_batch_stride, codes,
+                          codes_stride, codes_batch_stride, scales, scales_stride,
+                          scales_batch_stride);
     }
-    window_write_kernel<<<grid_for(rows * d, 256), 256, 0, stream>>>(
-        (const __nv_bfloat16*)x, nbatch, seqlen, d, x_stride, start_pos, window,
-        (__nv_bfloat16*)ring_rt, rt_stride, rt_batch_stride, codes, codes_stride, codes_batch_stride,
-        scales, scales_stride, scales_batch_stride);
-    return cudaGetLastError();
+    return launch_pdl(window_write_kernel, dim3(grid_for(rows * d, 256)), dim3(256), 0, stream,
+                      (const __nv_bfloat16*)x, nbatch, seqlen, d, x_stride, start_pos, window,
+                      (__nv_bfloat16*)ring_rt, rt_stride, rt_batch_stride, codes, codes_stride,
+                      codes_batch_stride, scales, scales_stride, scales_batch_stride);
 }
 
 }  // namespace sa

@@ -77,6 +77,34 @@ cudaError_t act_quant_launch(const void* x, int64_t n, int d, int64_t x_stride, 
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Programmatic dependent launches.  The kernels of one sparse_attn step (window table, act_quant
+// or ring write, attention, split merge) are launched so that each may be scheduled while the
+// work queued before it on the stream drains.  A kernel so launched may do set-up that touches
+// no global memory (barriers, TMEM, shared memory), must call pdl_wait() before its first global
+// read or write (it returns once every earlier grid on the stream has completed and its writes
+// are visible; with no such grid it returns at once), and calls pdl_trigger() to let the launch
+// after it be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <class Kernel, class... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Routing (sa_api.cu): the family a call runs in (SA_FAMILY_AUTO resolved; -1 = that family
 // cannot run the shape), and the workspace bytes that family needs for the shape.
 int routed_family(int family, int h, int d, int kv_format, int64_t b, int64_t rows);
