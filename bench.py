@@ -62,9 +62,12 @@ HEAD_START_CYCLES = 400_000
 # kernels are compiled from, workload).  Any change to those files makes the key miss, so a stale
 # figure reads as null.
 NCU_TRAFFIC = {
-    ("ea7a20fce0aa8291", "swa_prefill"): 500_166_656,
-    ("ea7a20fce0aa8291", "cmp_prefill"): 1_066_483_456,
-    ("ea7a20fce0aa8291", "decode"): 82_971_648,
+    ("c196db4413b0db0f", "swa_prefill"): 496_933_888,
+    ("c196db4413b0db0f", "cmp_prefill"): 1_062_592_768,
+    ("c196db4413b0db0f", "decode"): 80_141_952,
+    # the 4.5 GB workload itself gets a one-pass launch list only: its traffic is that of a
+    # 160-sequence capture (unsplit, like the full batch) times 256 / 160
+    ("c196db4413b0db0f", "fp8_decode"): 392_531_354,
 }
 
 

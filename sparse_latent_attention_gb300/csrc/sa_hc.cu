@@ -5,9 +5,10 @@
 // One thread per token.  A block's 256 rows of mixes are staged through shared memory (a
 // coalesced copy in, one padded row per thread), computed in registers in f32, and the outputs
 // leave through the same buffer as coalesced stores.  96 bytes in and 96 out per token at hc = 4;
-// a normalisation takes one IEEE reciprocal of its sum and multiplies (the page divides each
-// entry: one more rounding per step), since the ~640 divisions a token would otherwise take
-// bound the kernel, not its bytes.
+// a normalisation takes one reciprocal of its sum and multiplies (the page divides each entry:
+// one more rounding per step), since the ~640 divisions a token would otherwise take bound the
+// kernel, not its bytes.  The reciprocal is the hardware's approximation refined by one
+// Newton-Raphson step (within about one ulp; the sums are positive and normal).
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -17,6 +18,15 @@
 namespace {
 
 constexpr int kTok = 256;  // tokens (threads) per block
+
+// 1 / x for a positive normal f32: y0 = rcp.approx(x) (relative error below 2^-22), then one
+// Newton-Raphson step for f(y) = 1 / y - x, y1 = y0 + y0 (1 - x y0), which squares the relative
+// error.
+__device__ __forceinline__ float recip(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return fmaf(y, fmaf(-x, y, 1.0f), y);
+}
 
 template <int HC>
 __global__ void __launch_bounds__(kTok)
@@ -66,7 +76,7 @@ __global__ void __launch_bounds__(kTok)
                 c[j][k] = expf(c[j][k] - mx);
                 sum += c[j][k];
             }
-            const float inv = 1.f / sum;
+            const float inv = recip(sum);
 #pragma unroll
             for (int k = 0; k < HC; ++k) c[j][k] = c[j][k] * inv + eps;
         }
@@ -79,7 +89,7 @@ __global__ void __launch_bounds__(kTok)
                     float sum = 0.f;
 #pragma unroll
                     for (int k = 0; k < HC; ++k) sum += c[j][k];
-                    const float inv = 1.f / (sum + eps);
+                    const float inv = recip(sum + eps);
 #pragma unroll
                     for (int k = 0; k < HC; ++k) c[j][k] *= inv;
                 }
@@ -89,7 +99,7 @@ __global__ void __launch_bounds__(kTok)
                 float sum = 0.f;
 #pragma unroll
                 for (int j = 0; j < HC; ++j) sum += c[j][k];
-                const float inv = 1.f / (sum + eps);
+                const float inv = recip(sum + eps);
 #pragma unroll
                 for (int j = 0; j < HC; ++j) c[j][k] *= inv;
             }
