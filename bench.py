@@ -651,29 +651,48 @@ def run_gpu(args, rank, world, local):
         path.step()
         pin["o"].copy_(path.o, non_blocking=True)
 
+    ev_cmp_all = torch.cuda.Event()                        # every compute of a step is done
+    ev_out = [torch.cuda.Event() for _ in parts]           # part i's copy out is done
+    ev_q = [torch.cuda.Event() for _ in parts]             # part i's queries are in
+    ev_in, ev_pro = torch.cuda.Event(), torch.cuda.Event()
+    started = [False]
+
     def e2e_step_parts():
+        """One step: the step's inputs in (idx, sink, the new kv rows, then the queries part by
+        part), the prologue, each part's attention and its copy out, on three streams.  A step's
+        copies in wait only for the previous step's computes (which read q, idx and kv), so they
+        overlap the previous step's last copies out; a part's attention also waits for that
+        part's previous copy out (o is reused)."""
         cur = torch.cuda.current_stream()
-        # the previous step's compute has read q, kv and idx, and its copies out have read o
-        cur.wait_stream(s_cmp)
-        cur.wait_stream(s_out)
-        s_in.wait_stream(cur)
-        path.new_rows.copy_(pin["rows"], non_blocking=True)
-        path.sink.copy_(pin["sink"], non_blocking=True)
-        if pin["idx"] is not None:
-            path.idx.copy_(pin["idx"], non_blocking=True)
+        s_in.wait_stream(cur)  # after the timing event and the previous step's prologue
+        if started[0]:
+            s_in.wait_event(ev_cmp_all)
+        with torch.cuda.stream(s_in):
+            if pin["idx"] is not None:
+                path.idx.copy_(pin["idx"], non_blocking=True)
+            path.sink.copy_(pin["sink"], non_blocking=True)
+            path.new_rows.copy_(pin["rows"], non_blocking=True)
+            ev_in.record()
+        cur.wait_event(ev_in)
         path.prologue()
-        s_cmp.wait_stream(cur)
-        for part in parts:
+        ev_pro.record(cur)
+        for i, part in enumerate(parts):
             qs = part[0]
             with torch.cuda.stream(s_in):
                 path.q[qs].copy_(pin["q"][qs], non_blocking=True)
-            s_cmp.wait_stream(s_in)
+                ev_q[i].record()
+            s_cmp.wait_event(ev_pro)
+            s_cmp.wait_event(ev_q[i])
+            if started[0]:
+                s_cmp.wait_event(ev_out[i])
             with torch.cuda.stream(s_cmp):
                 path.attn(part, ws_parts)
             s_out.wait_stream(s_cmp)
             with torch.cuda.stream(s_out):
                 pin["o"][qs].copy_(path.o[qs], non_blocking=True)
-        cur.wait_stream(s_out)
+                ev_out[i].record()
+        ev_cmp_all.record(s_cmp)
+        started[0] = True
 
     e2e_step = e2e_step_parts if len(parts) > 1 else e2e_step_serial
 
@@ -686,10 +705,17 @@ def run_gpu(args, rank, world, local):
     e0.record()
     for _ in range(e2e_steps):
         e2e_step()
+    # the last step's copies out (on their own stream) are inside the timed region
+    torch.cuda.current_stream().wait_stream(s_out)
     e1.record()
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # the overlapped end-to-end step read back what a plain step computes, bit for bit
+    path.step()
+    torch.cuda.synchronize()
+    assert torch.equal(pin["o"].view(torch.int16), path.o.cpu().view(torch.int16)), \
+        "end-to-end output differs from the device step"
 
     # the other workloads, each timed alone the same way (device time only; rank 0's GPU line
     # carries them, every rank runs them so the ranks stay in step)
