@@ -555,3 +555,47 @@ def test_resident_rows_not_reused_across_sequences(dev, b, s, start_pos, rows, t
         torch.cuda.synchronize()
         assert sa.read_status(ws) == 0
         assert_close_bf16(_gpu.bf16_tensor_to_u16(o2), want, ATOL, RTOL, what=f"reuse, run {rep + 2}")
+
+
+def test_decode_step_replays_from_a_cuda_graph(dev):
+    """A decode step -- the window table, the ring write of the step's new rows, and sparse_attn with
+    its split merge (programmatic dependent launches) -- captured once into a CUDA graph and
+    replayed: the same bits as the eager calls, replay after replay, with new inputs copied into
+    the captured buffers between replays."""
+    b, d, window, rows, topk, pos = 6, 512, 128, 3000, 1152, 4321
+    wl = workloads.make_random(b, 1, 64, d, rows, topk, seed=8080, window=window, start_pos=pos)
+    x = _gpu.prepare(wl, dev, quantise=True)
+    new_rows = torch.randn((b, 1, d), device=dev).to(torch.bfloat16)
+    ws = sa.new_workspace(b, 1, 64, d, rows, topk, device=dev)
+    out = torch.empty_like(x["q"])
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        sa.window_idxs(pos, 1, window, out=x["idx"][:, :, :window], nbatch=b)
+        sa.window_write(new_rows, pos, ring_rt=x["kv"][:, :window])
+        sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, out=out, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        step()  # eager, also configures the kernels before the capture
+    torch.cuda.synchronize()
+    eager = out.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for rep in range(3):
+        out.fill_(0)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16)), f"replay {rep}"
+    # new queries copied into the captured buffer: the replay follows them
+    x["q"].copy_(torch.randn_like(x["q"], dtype=torch.float32).to(torch.bfloat16))
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    eager2 = out.clone()
+    out.fill_(0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager2.view(torch.int16))
+    assert not torch.equal(eager2.view(torch.int16), eager.view(torch.int16))
+    assert sa.read_status(ws) == 0
