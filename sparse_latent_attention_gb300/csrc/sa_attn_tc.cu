@@ -19,11 +19,12 @@
 // so the rescale is rare.  The sink joins the denominator once, in the epilogue:
 // o = O / (l + 2^(sink log2e - m)).
 //
-// Roles (persistent CTAs, one 64-head block of one query token per task, 448 threads):
-//   warp 0      MMA issue (one elected lane) and TMEM allocation; the next logits and the next
-//               P.V are each issued as soon as they are ready (the P.V first when both are), so
-//               the gather of one buffer, the logits of its tile and the softmax and P.V of the
-//               other tile overlap
+// Roles (persistent CTAs, one 64-head block of one query token per task, 480 threads):
+//   warp 0      logits issue (one elected lane) and TMEM allocation
+//   warp 14     P.V issue (one elected lane).  Two issuing warps, each blocked on its own
+//               barriers, keep one product's bookkeeping off the other's path: the tensor pipe
+//               takes the MMAs of both as they come, so the gather of one buffer, the logits of
+//               its tile and the softmax and P.V of the other tile overlap
 //   warp 1      Q loads (TMA, 128-byte swizzle) and an L2 prefetch of the next task's Q
 //   warps 2-5   kv row gather: the 128 idx columns of a pair of tiles at a time, one per thread;
 //               cp.async 16 B into the swizzled layout (fp8 rows are staged raw and widened in
@@ -66,7 +67,8 @@ constexpr int kProdWarps = 4;                       // kv gather warps (one pair
 constexpr int kProdThreads = 32 * kProdWarps;       // = the 128 columns of a pair of tiles
 constexpr int kWarpSoftmax = 2 + kProdWarps;        // first softmax warp
 constexpr int kWarpEpilogue = kWarpSoftmax + 4;     // first epilogue warp
-constexpr int kThreads = 32 * (kWarpEpilogue + 4);
+constexpr int kWarpPv = kWarpEpilogue + 4;         // P.V issue
+constexpr int kThreads = 32 * (kWarpPv + 1);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // TMEM columns: O^T chunks (4 x 64), the two S buffers (2 x 64)
@@ -226,6 +228,12 @@ __device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t& phase, volatile 
     return ok;
 }
 
+// A 16-byte cp.async at constant offsets from a shared and a global base address.
+template <uint32_t kSOff, int kGOff>
+__device__ __forceinline__ void cp_async16_at(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;" ::"r"(dst), "l"(src), "n"(kSOff), "n"(kGOff));
+}
+
 // Byte offset, inside the kv buffers, of 16-byte unit u (of 64) of the row in slot ps (bit 6 =
 // the buffer, bits 0-5 = the row of the tile): 64-d block u / 8, 128-byte swizzle.
 __device__ __forceinline__ uint32_t kv_unit_off(int ps, int u) {
@@ -311,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kChunks; ++c) mbar_init(smem_addr(&M.o_empty[c]), 128);
         mbar_init(smem_addr(&M.sm_bar), 128);
         mbar_init(smem_addr(&M.pr_bar), kProdThreads);
-        mbar_init(smem_addr(&M.done), 1);
+        mbar_init(smem_addr(&M.done), 2);
         M.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -345,133 +353,93 @@ __global__ void __launch_bounds__(kThreads, 1)
     task_range(p, tb, te);
 
     if (warp == 0) {
-        // ------------------------------------------------------------------ MMA issue
+        // ------------------------------------------------------------------ logits issue
         // The whole warp runs this loop (descriptors stay in uniform registers); each MMA and
         // commit is issued by one elected lane, and every lane waits on the barriers.  A wait's
         // result is made warp-uniform so that a time-out cannot split the warp.
         constexpr uint32_t id_s = idesc_bf16_f32(kHeads, kRows, false, false);
-        constexpr uint32_t id_o = idesc_bf16_f32(128, kHeads, true, false);
-        // base descriptors; the per-instruction ones add a start-address offset (>> 4)
-        const uint64_t a_s0 = smem_desc_sw128(s_q, 16, 1024);          // Q, K-major
-        const uint64_t b_s0 = smem_desc_sw128(s_kv, 16, 1024);         // tile rows, K-major
-        const uint64_t a_o0 = smem_desc_sw128(s_kv, kDBlkBytes, 1024);  // tile^T, MN-major
-        const uint64_t b_o0 = smem_desc_sw128(s_p, 16, 1024);          // P, K-major
-        // O^T += KV^T . P^T for tile pt (pt & 1 = its kv and P buffer) of task kk
-        auto issue_pv = [&](uint32_t pt, bool first, bool last, int64_t kk) -> bool {
-            const uint32_t b = pt & 1;
-            if (!warp_wait(smem_addr(&M.p_full[b]), (pt >> 1) & 1, abort)) return false;
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-                if (first) {  // the epilogue has read this chunk of the last task's O
-                    if (!warp_wait(smem_addr(&M.o_empty[c]), (uint32_t)(kk & 1) ^ 1, abort)) return false;
-                    tc_fence_after();
-                }
-                // K step ks = rows 16 ks .. 16 ks + 15 (2 KB of the two 64-d blocks of chunk c)
-#pragma unroll
-                for (int ks = 0; ks < kRows / 16; ++ks)
-                    mma_bf16_ss_elect(tmem + kColO + 64 * c,
-                                      a_o0 + (uint64_t)(b * (kBlkBytes >> 4) + c * (2 * kDBlkBytes >> 4) +
-                                                        ks * (16 * 128 >> 4)),
-                                      b_o0 + (uint64_t)(b * (kPBytes >> 4) + ks * 2), id_o,
-                                      !(first && ks == 0));
-            }
-            mma_commit_elect(smem_addr(&M.kv_empty[b]));  // the tile's rows are read
-            mma_commit_elect(smem_addr(&M.p_empty[b]));
-            if (last) mma_commit_elect(smem_addr(&M.o_full));
-            return true;
-        };
+        const uint64_t a_s0 = smem_desc_sw128(s_q, 16, 1024);   // Q, K-major
+        const uint64_t b_s0 = smem_desc_sw128(s_kv, 16, 1024);  // tile rows, K-major
         bool ok = true;
-        if (p.n_tiles == 0) {
-            // every task is empty (no idx columns): keep every phase in step
-            int64_t k = 0;
-            for (int64_t tau = tb; tau < te && ok; ++tau, ++k) {
-                const uint32_t kp = (uint32_t)(k & 1);
-                ok = warp_wait(smem_addr(&M.q_full), kp, abort);
+        int64_t k = 0;
+        uint32_t T = 0;
+        Task t = task_of(p, tb);
+        for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
+            if (p.n_tiles == 0) {  // no idx columns: keep the Q phases in step
+                ok = warp_wait(smem_addr(&M.q_full), (uint32_t)(k & 1), abort);
                 mma_commit_elect(smem_addr(&M.q_empty));
-                for (int c = 0; c < kChunks && ok; ++c)
-                    ok = warp_wait(smem_addr(&M.o_empty[c]), kp ^ 1, abort);
-                mma_commit_elect(smem_addr(&M.o_full));
+                continue;
             }
-        } else {
-            // Two cursors over the CTA's tiles (every task has at least one): the next logits
-            // and the next P.V.  Whichever is ready is issued, the P.V first (it releases a kv
-            // buffer to the gather); the logits of a tile can so run during the softmax of the
-            // one before.  Readiness is polled without blocking; the poll is bounded.
-            struct Cursor {
-                Task t;
-                int64_t tau, k;
-                int ti;
-                uint32_t T;
-            };
-            auto advance = [&](Cursor& c) {
-                ++c.T;
-                if (++c.ti == c.t.t1) {
-                    ++c.tau;
-                    ++c.k;
-                    task_step(p, c.t);
-                    c.ti = c.t.t0;
-                }
-            };
-            Cursor cs;
-            cs.t = task_of(p, tb);
-            cs.tau = tb;
-            cs.k = 0;
-            cs.ti = cs.t.t0;
-            cs.T = 0;
-            Cursor cv = cs;
-            uint32_t idle = 0;
-            while (cv.tau < te) {
-                bool did = false;
-                if (cv.T < cs.T &&
-                    __all_sync(0xffffffffu, mbar_test_wait(smem_addr(&M.p_full[cv.T & 1]), (cv.T >> 1) & 1))) {
-                    if (!(ok = issue_pv(cv.T, cv.ti == cv.t.t0, cv.ti == cv.t.t1 - 1, cv.k))) break;
-                    advance(cv);
-                    did = true;
-                } else if (cs.tau < te) {
-                    const uint32_t b = cs.T & 1, use = cs.T >> 1;
-                    const bool first = cs.ti == cs.t.t0;
-                    const bool rdy = mbar_test_wait(smem_addr(&M.s_empty[b]), (use & 1) ^ 1) &&
-                                     mbar_test_wait(smem_addr(&M.kv_full[b]), use & 1) &&
-                                     (!first || mbar_test_wait(smem_addr(&M.q_full), (uint32_t)(cs.k & 1)));
-                    if (__all_sync(0xffffffffu, rdy)) {
-                        tc_fence_after();
-                        // S = Q . tile^T: K step 4 kb + kq (16 of 512) = block kb of Q and of the
-                        // tile, 32 B per step inside a 128-byte row (the block loop is kept rolled:
-                        // the issuing warp shares its instruction cache with three other roles)
-                        const uint32_t s_col = tmem + kColS + 64 * b;
-                        const uint64_t b_sb = b_s0 + (uint64_t)(b * (kBlkBytes >> 4));
+            for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
+                const uint32_t b = T & 1, use = T >> 1;
+                ok = warp_wait(smem_addr(&M.kv_full[b]), use & 1, abort) &&
+                     warp_wait(smem_addr(&M.s_empty[b]), (use & 1) ^ 1, abort) &&
+                     (ti != t.t0 || warp_wait(smem_addr(&M.q_full), (uint32_t)(k & 1), abort));
+                if (!ok) break;
+                tc_fence_after();
+                // S = Q . tile^T: K step 4 kb + kq (16 of 512) = block kb of Q and of the tile,
+                // 32 B per step inside a 128-byte row
+                const uint32_t s_col = tmem + kColS + 64 * b;
+                const uint64_t b_sb = b_s0 + (uint64_t)(b * (kBlkBytes >> 4));
 #pragma unroll 1
-                        for (int kb = 0; kb < 8; ++kb) {
+                for (int kb = 0; kb < 8; ++kb) {
 #pragma unroll
-                            for (int kq = 0; kq < 4; ++kq)
-                                mma_bf16_ss_elect(s_col, a_s0 + (uint64_t)(kb * (kQBlkBytes >> 4) + kq * 2),
-                                                  b_sb + (uint64_t)(kb * (kDBlkBytes >> 4) + kq * 2), id_s,
-                                                  (kb | kq) != 0);
-                        }
-                        if (cs.ti == cs.t.t1 - 1) mma_commit_elect(smem_addr(&M.q_empty));
-                        mma_commit_elect(smem_addr(&M.s_full[b]));
-                        advance(cs);
-                        did = true;
-                    }
+                    for (int kq = 0; kq < 4; ++kq)
+                        mma_bf16_ss_elect(s_col, a_s0 + (uint64_t)(kb * (kQBlkBytes >> 4) + kq * 2),
+                                          b_sb + (uint64_t)(kb * (kDBlkBytes >> 4) + kq * 2), id_s,
+                                          (kb | kq) != 0);
                 }
-                if (did) {
-                    idle = 0;
-                } else {
-                    if (__any_sync(0xffffffffu, *abort != 0)) {
-                        ok = false;
-                        break;
-                    }
-                    if (++idle > (1u << 22)) {  // nothing became ready for a very long time
-                        *abort = 1;
-                        ok = false;
-                        break;
-                    }
-                    if (idle > 64) __nanosleep(32);
-                }
+                if (ti == t.t1 - 1) mma_commit_elect(smem_addr(&M.q_empty));
+                mma_commit_elect(smem_addr(&M.s_full[b]));
             }
         }
         // let every issued MMA finish before the accumulators are released
+        mma_commit_elect(smem_addr(&M.done));
+        warp_wait(smem_addr(&M.done), 0, abort);
+    } else if (warp == kWarpPv) {
+        // ------------------------------------------------------------------ P.V issue
+        constexpr uint32_t id_o = idesc_bf16_f32(128, kHeads, true, false);
+        const uint64_t a_o0 = smem_desc_sw128(s_kv, kDBlkBytes, 1024);  // tile^T, MN-major
+        const uint64_t b_o0 = smem_desc_sw128(s_p, 16, 1024);           // P, K-major
+        bool ok = true;
+        int64_t k = 0;
+        uint32_t T = 0;
+        Task t = task_of(p, tb);
+        for (int64_t tau = tb; tau < te && ok; ++tau, ++k, task_step(p, t)) {
+            if (p.n_tiles == 0) {  // no idx columns: keep the O phases in step
+                for (int c = 0; c < kChunks && ok; ++c)
+                    ok = warp_wait(smem_addr(&M.o_empty[c]), (uint32_t)(k & 1) ^ 1, abort);
+                mma_commit_elect(smem_addr(&M.o_full));
+                continue;
+            }
+            for (int ti = t.t0; ti < t.t1 && ok; ++ti, ++T) {
+                // O^T += KV^T . P^T for tile T (T & 1 = its kv and P buffer)
+                const uint32_t b = T & 1;
+                const bool first = ti == t.t0;
+                if (!(ok = warp_wait(smem_addr(&M.p_full[b]), (T >> 1) & 1, abort))) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < kChunks && ok; ++c) {
+                    if (first) {  // the epilogue has read this chunk of the last task's O
+                        if (!(ok = warp_wait(smem_addr(&M.o_empty[c]), (uint32_t)(k & 1) ^ 1, abort))) break;
+                        tc_fence_after();
+                    }
+                    // K step ks = rows 16 ks .. 16 ks + 15 (2 KB of the two 64-d blocks of chunk c)
+#pragma unroll
+                    for (int ks = 0; ks < kRows / 16; ++ks)
+                        mma_bf16_ss_elect(tmem + kColO + 64 * c,
+                                          a_o0 + (uint64_t)(b * (kBlkBytes >> 4) + c * (2 * kDBlkBytes >> 4) +
+                                                            ks * (16 * 128 >> 4)),
+                                          b_o0 + (uint64_t)(b * (kPBytes >> 4) + ks * 2), id_o,
+                                          !(first && ks == 0));
+                }
+                if (!ok) break;
+                mma_commit_elect(smem_addr(&M.kv_empty[b]));  // the tile's rows are read
+                mma_commit_elect(smem_addr(&M.p_empty[b]));
+                if (ti == t.t1 - 1) mma_commit_elect(smem_addr(&M.o_full));
+            }
+        }
+        // (done completes once both issuing warps' MMAs have)
         mma_commit_elect(smem_addr(&M.done));
         warp_wait(smem_addr(&M.done), 0, abort);
     } else if (warp == 1) {
@@ -692,26 +660,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             st_shared_v4(s_kv + kv_unit_off(r, 32 + lane), w1.x, w1.y, w1.z, w1.w);
                         }
                     } else {
-                        // entries e0 + lane / 16 + 2 i (two rows per instruction); 16-byte unit
-                        // lane % 16 of each 256-byte quarter of the row
+                        // list entries lane / 16 + 2 i (two rows per instruction); lane % 16 moves
+                        // 16-byte unit u = 16 c + lane % 16 of quarter c of the row.  One shared and
+                        // one global base address per row, the quarters at constant offsets: unit u
+                        // sits in 64-d block u / 8 = 2 c + (lane % 16) / 8 at swizzled position
+                        // (lane % 8) ^ (slot % 8), i.e. bits 4-6 of the 1024-byte aligned base
+                        // (the instruction count of this loop bounds the gather)
+                        const uint32_t s_lane = s_kv + (uint32_t)((lane & 15) >> 3) * kDBlkBytes +
+                                                ((uint32_t)lane & 7) * 16;
+                        const char* g_lane = reinterpret_cast<const char*>(kvb) + (lane & 15) * 16;
 #pragma unroll 1
-                        for (int e0 = 0; e0 < ncopy; e0 += 8) {
-                            int2 ent[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int e = e0 + (lane >> 4) + 2 * i;
-                                ent[i] = e < ncopy ? M.copy_list[pw][hx][e] : make_int2(-1, 0);
-                            }
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const int u = 16 * c + (lane & 15);
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    if (ent[i].x < 0) break;
-                                    cp_async16(s_kv + kv_unit_off(ent[i].y, u),
-                                               kvb + (int64_t)ent[i].x * kD + u * 8, 16u);
-                                }
-                            }
+                        for (int e = lane >> 4; e < ncopy; e += 2) {
+                            const int2 en = M.copy_list[pw][hx][e];
+                            const uint32_t ps = (uint32_t)en.y;
+                            const uint32_t sb = (s_lane ^ ((ps & 7) << 4)) + (ps >> 6) * kBlkBytes +
+                                                (ps & 63) * 128;
+                            const char* gb = g_lane + (int64_t)en.x * (kD * 2);
+                            cp_async16_at<0, 0>(sb, gb);
+                            cp_async16_at<2 * kDBlkBytes, 256>(sb, gb);
+                            cp_async16_at<4 * kDBlkBytes, 512>(sb, gb);
+                            cp_async16_at<6 * kDBlkBytes, 768>(sb, gb);
                         }
                         cp_async_commit();
                         cp_async_wait<0>();
@@ -754,12 +722,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(smem_addr(&M.s_empty[b]));
                 // scaled logits (log2 units); an unclaimed slot's become -inf
                 const uint32_t vm = reinterpret_cast<const uint32_t*>(M.vmask16[b])[hf];
-                float x[32];
-                float mt = -INFINITY;
+                // every one of the 32 slots claimed (the usual case): the maximum of the raw logits
+                // (the minimum for a negative scale) times the scale, and p = 2^(s scale - m) in one
+                // FMA; otherwise the scaled logits replace the raw ones, -inf where unclaimed
+                const bool full = vm == 0xFFFFFFFFu;
+                float mt, sc = p.scale_log2;
+                if (full) {
+                    float a = __uint_as_float(r[0]);
+                    if (sc >= 0.f) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    x[i] = ((vm >> i) & 1u) ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
-                    mt = fmaxf(mt, x[i]);
+                        for (int i = 1; i < 32; ++i) a = fmaxf(a, __uint_as_float(r[i]));
+                    } else {
+#pragma unroll
+                        for (int i = 1; i < 32; ++i) a = fminf(a, __uint_as_float(r[i]));
+                    }
+                    mt = a * sc;
+                } else {
+                    mt = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float xi = ((vm >> i) & 1u) ? __uint_as_float(r[i]) * sc : -INFINITY;
+                        r[i] = __float_as_uint(xi);
+                        mt = fmaxf(mt, xi);
+                    }
+                    sc = 1.f;
                 }
                 mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
                 float al = 1.f, mn = mt;
@@ -779,7 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float ps = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float e0 = fast_exp2(x[2 * i] - mu), e1 = fast_exp2(x[2 * i + 1] - mu);
+                    const float e0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), sc, -mu));
+                    const float e1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), sc, -mu));
                     ps += e0 + e1;
                     pk[i] = pack_bf16(e0, e1);
                 }
