@@ -135,32 +135,9 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
-// Tiled 3-D store of a shared-memory box to global memory (bulk async-group completion).  The
-// box is clipped at the tensor's extents; the start coordinates must not be negative.
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t x, int32_t y,
-                                             int32_t z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-            tmap),
-        "r"(src), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// every committed bulk store has finished reading its shared-memory source
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// every committed bulk store has completed
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Starts pulling `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// Starts pulling the 128-byte line holding `p` into L2 (a load/store-unit prefetch).
-__device__ __forceinline__ void prefetch_line_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
