@@ -238,8 +238,23 @@ __device__ __forceinline__ uint32_t kv_unit_off(int ps, int u) {
 // x < 0 = none); the row's 16 e8m0 scales are in fp8_sc.
 __device__ __forceinline__ void widen_fp8(uint32_t s_kv, const Misc& M, const int2 (&ent)[8], int unit,
                                           int c0, int c1) {
+    // Per entry, once: the slot's offset inside a 64-d block (buffer and row) and the byte offset
+    // of this lane's first bf16 unit in it.  Unit u = 16 c + 2 unit of the row sits in block
+    // u / 8 = 2 c + unit / 4 at swizzled position (u % 8) ^ (slot % 8), u % 8 = 2 (unit % 4); unit
+    // u + 1 is the same address with bit 4 flipped (u is even).
+    uint32_t rb[8], xo[8];
+    const uint32_t uo = (uint32_t)(2 * (unit & 3)) << 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t r = (uint32_t)ent[i].y;
+        rb[i] = (r >> 6) * kBlkBytes + (r & 63) * 128;
+        xo[i] = rb[i] + (uo ^ ((r & 7) << 4));
+    }
+    const uint8_t* sc_base = &M.fp8_sc[0][0] + (unit >> 1);
 #pragma unroll 1
     for (int cw = c0; cw < c1; ++cw) {
+        const uint32_t code_at = s_kv + (2 * cw + 1) * kDBlkBytes + unit * 16;
+        const uint32_t out_at = s_kv + (2 * cw + (unit >> 2)) * kDBlkBytes;
         // entries in two groups of four; a row's 8 lanes read all its codes before any writes
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
@@ -249,25 +264,22 @@ __device__ __forceinline__ void widen_fp8(uint32_t s_kv, const Misc& M, const in
             for (int i = 0; i < 4; ++i) {
                 const int2 en = ent[4 * g + i];
                 if (en.x < 0) break;
-                const int r = en.y;
                 asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                              : "=r"(code[i].x), "=r"(code[i].y), "=r"(code[i].z), "=r"(code[i].w)
-                             : "r"(s_kv + (2 * cw + 1) * kDBlkBytes + (uint32_t)(r >> 6) * kBlkBytes +
-                                   (uint32_t)(r & 63) * 128 + unit * 16)
+                             : "r"(code_at + rb[4 * g + i])
                              : "memory");
-                sc[i] = fp8::e8m0_to_f32(M.fp8_sc[r][4 * cw + (unit >> 1)]);
+                sc[i] = fp8::e8m0_to_f32(sc_base[en.y * 16 + 4 * cw]);
             }
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int2 en = ent[4 * g + i];
                 if (en.x < 0) break;
-                const int r = en.y;
                 uint4 lo, hi;
                 fp8::dequant16(code[i], sc[i], lo, hi);
-                const int u = 16 * cw + 2 * unit;  // 16-byte bf16 units u, u + 1
-                st_shared_v4(s_kv + kv_unit_off(r, u), lo.x, lo.y, lo.z, lo.w);
-                st_shared_v4(s_kv + kv_unit_off(r, u + 1), hi.x, hi.y, hi.z, hi.w);
+                const uint32_t at = out_at + xo[4 * g + i];
+                st_shared_v4(at, lo.x, lo.y, lo.z, lo.w);
+                st_shared_v4(at ^ 16u, hi.x, hi.y, hi.z, hi.w);
             }
         }
     }
