@@ -594,16 +594,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int2 en = M.copy_list[pw][hx][lane];
                             cp_async16(smem_addr(&M.fp8_sc[en.y][0]), scb + (int64_t)en.x * (kD / 32), 16u);
                         }
+                        // per row one shared and one global base, chunk c at constant offsets
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                if (ent8[i].x < 0) break;
-                                const int r = ent8[i].y;
-                                cp_async16(s_kv + (2 * c + 1) * kDBlkBytes + (uint32_t)(r >> 6) * kBlkBytes +
-                                               (uint32_t)(r & 63) * 128 + unit * 16,
-                                           kvb8 + (int64_t)ent8[i].x * kD + 128 * c + unit * 16, 16u);
-                            }
+                        for (int i = 0; i < 8; ++i) {
+                            if (ent8[i].x < 0) break;
+                            const uint32_t r = (uint32_t)ent8[i].y;
+                            const uint32_t sb = s_kv + kDBlkBytes + (r >> 6) * kBlkBytes + (r & 63) * 128 + unit * 16;
+                            const uint8_t* gb = kvb8 + (int64_t)ent8[i].x * kD + unit * 16;
+                            cp_async16_at<0, 0>(sb, gb);
+                            cp_async16_at<2 * kDBlkBytes, 128>(sb, gb);
+                            cp_async16_at<4 * kDBlkBytes, 256>(sb, gb);
+                            cp_async16_at<6 * kDBlkBytes, 384>(sb, gb);
                         }
                         cp_async_commit();
                     }
