@@ -62,12 +62,12 @@ HEAD_START_CYCLES = 400_000
 # kernels are compiled from, workload).  Any change to those files makes the key miss, so a stale
 # figure reads as null.
 NCU_TRAFFIC = {
-    ("9d1dcb2db1e07006", "swa_prefill"): 495_602_745,
-    ("9d1dcb2db1e07006", "cmp_prefill"): 1_061_941_589,
-    ("9d1dcb2db1e07006", "decode"): 80_155_922,
+    ("0bde6ad4706d7dec", "swa_prefill"): 495_711_943,
+    ("0bde6ad4706d7dec", "cmp_prefill"): 1_062_150_599,
+    ("0bde6ad4706d7dec", "decode"): 80_252_635,
     # the 4.5 GB workload itself gets a one-pass launch list only: its traffic is that of a
     # 160-sequence capture (unsplit, like the full batch) times 256 / 160
-    ("9d1dcb2db1e07006", "fp8_decode"): 387_871_642,
+    ("0bde6ad4706d7dec", "fp8_decode"): 387_756_442,
 }
 
 
