@@ -206,6 +206,62 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Three-input maximum and minimum, and f32 pairs (two lanes of one 64-bit register) for the packed
+// FMA and add.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// The maximum (kMax) or minimum of 32 raw f32 words, as a tree of three-input operations.
+template <bool kMax>
+__device__ __forceinline__ float reduce32(const uint32_t (&r)[32]) {
+    auto op3 = [](float a, float b, float c) { return kMax ? max3f(a, b, c) : min3f(a, b, c); };
+    auto op2 = [](float a, float b) { return kMax ? fmaxf(a, b) : fminf(a, b); };
+    float a[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i)
+        a[i] = op3(__uint_as_float(r[3 * i]), __uint_as_float(r[3 * i + 1]), __uint_as_float(r[3 * i + 2]));
+    a[10] = op2(__uint_as_float(r[30]), __uint_as_float(r[31]));
+    const float b0 = op3(a[0], a[1], a[2]), b1 = op3(a[3], a[4], a[5]), b2 = op3(a[6], a[7], a[8]);
+    return op3(b0, b1, op3(b2, a[9], a[10]));
+}
+
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t pack_bf16_2(uint64_t v) {
+    float lo, hi;
+    f2_split(v, lo, hi);
+    return pack_bf16(lo, hi);
+}
+
 // mbar_wait by every lane of a converged warp, with a warp-uniform result.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
@@ -222,7 +278,8 @@ __device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t& phase, volatile 
 // A 16-byte cp.async at constant offsets from a shared and a global base address.
 template <uint32_t kSOff, int kGOff>
 __device__ __forceinline__ void cp_async16_at(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;" ::"r"(dst), "l"(src), "n"(kSOff), "n"(kGOff));
+    asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;" ::"r"(dst), "l"(src), "n"(kSOff),
+                 "n"(kGOff));
 }
 
 // Byte offset, inside the kv buffers, of 16-byte unit u (of 64) of the row in slot ps (bit 6 =
@@ -381,14 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // S = Q . tile^T: K step 4 kb + kq (16 of 512) = block kb of Q and of the tile,
                 // 32 B per step inside a 128-byte row
                 const uint32_t s_col = tmem + kColS + 64 * b;
-                const uint64_t b_sb = b_s0 + (uint64_t)(b * (kBlkBytes >> 4));
+                const uint32_t ahi = (uint32_t)(a_s0 >> 32), bhi = (uint32_t)(b_s0 >> 32);
+                uint32_t alo = (uint32_t)a_s0, blo = (uint32_t)b_s0 + b * (kBlkBytes >> 4);
 #pragma unroll 1
                 for (int kb = 0; kb < 8; ++kb) {
 #pragma unroll
                     for (int kq = 0; kq < 4; ++kq)
-                        mma_bf16_ss_elect(s_col, a_s0 + (uint64_t)(kb * (kQBlkBytes >> 4) + kq * 2),
-                                          b_sb + (uint64_t)(kb * (kDBlkBytes >> 4) + kq * 2), id_s,
-                                          (kb | kq) != 0);
+                        mma_lohi_elect(s_col, alo + kq * 2, ahi, blo + kq * 2, bhi, id_s, (kb | kq) != 0);
+                    alo += kQBlkBytes >> 4;
+                    blo += kDBlkBytes >> 4;
                 }
                 if (ti == t.t1 - 1) mma_commit_elect(smem_addr(&M.q_empty));
                 mma_commit_elect(smem_addr(&M.s_full[b]));
@@ -426,13 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                     }
                     // K step ks = rows 16 ks .. 16 ks + 15 (2 KB of the two 64-d blocks of chunk c)
+                    const uint32_t alo = (uint32_t)a_o0 + b * (kBlkBytes >> 4) + c * (2 * kDBlkBytes >> 4);
+                    const uint32_t blo = (uint32_t)b_o0 + b * (kPBytes >> 4);
+                    const uint32_t ahi = (uint32_t)(a_o0 >> 32), bhi = (uint32_t)(b_o0 >> 32);
 #pragma unroll
                     for (int ks = 0; ks < kRows / 16; ++ks)
-                        mma_bf16_ss_elect(tmem + kColO + 64 * c,
-                                          a_o0 + (uint64_t)(b * (kBlkBytes >> 4) + c * (2 * kDBlkBytes >> 4) +
-                                                            ks * (16 * 128 >> 4)),
-                                          b_o0 + (uint64_t)(b * (kPBytes >> 4) + ks * 2), id_o,
-                                          !(first && ks == 0));
+                        mma_lohi_elect(tmem + kColO + 64 * c, alo + ks * (16 * 128 >> 4), ahi, blo + ks * 2,
+                                       bhi, id_o, !(first && ks == 0));
                 }
                 if (!ok) break;
                 mma_commit_elect(smem_addr(&M.kv_empty[b]));  // the tile's rows are read
@@ -599,7 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 8; ++i) {
                             if (ent8[i].x < 0) break;
                             const uint32_t r = (uint32_t)ent8[i].y;
-                            const uint32_t sb = s_kv + kDBlkBytes + (r >> 6) * kBlkBytes + (r & 63) * 128 + unit * 16;
+                            const uint32_t sb =
+                                s_kv + kDBlkBytes + (r >> 6) * kBlkBytes + (r & 63) * 128 + unit * 16;
                             const uint8_t* gb = kvb8 + (int64_t)ent8[i].x * kD + unit * 16;
                             cp_async16_at<0, 0>(sb, gb);
                             cp_async16_at<2 * kDBlkBytes, 128>(sb, gb);
@@ -730,15 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool full = vm == 0xFFFFFFFFu;
                 float mt, sc = p.scale_log2;
                 if (full) {
-                    float a = __uint_as_float(r[0]);
-                    if (sc >= 0.f) {
-#pragma unroll
-                        for (int i = 1; i < 32; ++i) a = fmaxf(a, __uint_as_float(r[i]));
-                    } else {
-#pragma unroll
-                        for (int i = 1; i < 32; ++i) a = fminf(a, __uint_as_float(r[i]));
-                    }
-                    mt = a * sc;
+                    mt = (sc >= 0.f ? reduce32<true>(r) : reduce32<false>(r)) * sc;
                 } else {
                     mt = -INFINITY;
 #pragma unroll
@@ -763,15 +814,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mu = mn == -INFINITY ? 0.f : mn;
                 // p = 2^(x - m): this thread's 32 columns are 16-byte units 4 hf .. 4 hf + 3 of
                 // the head's 128-byte P row (swizzled like every K-major operand)
+                // (pairs of columns through the packed FMA and add; two running pair sums)
                 uint32_t pk[16];
-                float ps = 0.f;
+                const uint64_t sc2 = f2(sc, sc), nm2 = f2(-mu, -mu);
+                uint64_t acc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float e0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), sc, -mu));
-                    const float e1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), sc, -mu));
-                    ps += e0 + e1;
+                    float x0, x1;
+                    const uint64_t s2 = f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    f2_split(ffma2(s2, sc2, nm2), x0, x1);
+                    const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                    acc[i & 1] = fadd2(acc[i & 1], f2(e0, e1));
                     pk[i] = pack_bf16(e0, e1);
                 }
+                float a0, a1, a2, a3;
+                f2_split(acc[0], a0, a1);
+                f2_split(acc[1], a2, a3);
+                const float ps = (a0 + a1) + (a2 + a3);
                 l = first ? ps : fmaf(al, l, ps);
                 // the P buffer is free once the P.V two tiles back has completed
                 if (!(ok = mbar_wait(smem_addr(&M.p_empty[b]), (use & 1) ^ 1, abort))) break;
@@ -962,10 +1021,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int mq = 0; mq < 8; ++mq) {
                         const float4 w = *reinterpret_cast<const float4*>(&M.inv[q4][32 * rh + 4 * mq]);
                         const int a = 32 * rh + 4 * mq;
-                        const uint32_t pk0 = pack_bf16(__uint_as_float(r[a]) * w.x,
-                                                       __uint_as_float(r[a + 1]) * w.y);
-                        const uint32_t pk1 = pack_bf16(__uint_as_float(r[a + 2]) * w.z,
-                                                       __uint_as_float(r[a + 3]) * w.w);
+                        // (pairs of heads scaled by one paired multiply: the same two products)
+                        const uint32_t pk0 = pack_bf16_2(
+                            fmul2(f2(__uint_as_float(r[a]), __uint_as_float(r[a + 1])), f2(w.x, w.y)));
+                        const uint32_t pk1 = pack_bf16_2(
+                            fmul2(f2(__uint_as_float(r[a + 2]), __uint_as_float(r[a + 3])), f2(w.z, w.w)));
                         out[2 * mq] = __byte_perm(pk0, __shfl_xor_sync(0xffffffffu, pk0, 1), sel);
                         out[2 * mq + 1] = __byte_perm(pk1, __shfl_xor_sync(0xffffffffu, pk1, 1), sel);
                     }
