@@ -559,9 +559,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // after this pair's barrier, when nobody reads it any more, and is next written
                 // by the pair after the next, after the next pair's barrier.  The next pair's
                 // own entry must not be touched here: a fast thread may be filling it already.)
-                if (j >= 0) {
-                    atomicOr(&M.ring_bits[g3][(j & 127) >> 5], 1u << (j & 31));
-                    atomicAdd(&M.ring_count[g3], 1);
+                {
+                    // per warp: the residue bits of each of the four words or-reduced, and the count
+                    // of valid rows, added by one lane
+                    const uint32_t w = (uint32_t)(j & 127) >> 5, bit = j >= 0 ? 1u << (j & 31) : 0u;
+                    uint32_t wb[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) wb[q] = __reduce_or_sync(0xffffffffu, w == (uint32_t)q ? bit : 0u);
+                    const uint32_t nv = (uint32_t)__popc(__ballot_sync(0xffffffffu, j >= 0));
+                    if (lane == 0) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (wb[q]) atomicOr(&M.ring_bits[g3][q], wb[q]);
+                        if (nv) atomicAdd(&M.ring_count[g3], (int)nv);
+                    }
                 }
                 if (pt == 0) M.pair_seq[g3] = bi;
                 if (!(ok = wg_sync(smem_addr(&M.pr_bar), pr_phase, abort))) break;
