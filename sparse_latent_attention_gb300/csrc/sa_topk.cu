@@ -230,7 +230,9 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
 }
 
 // Launch a per-row kernel with `keys` 32-bit keys of shared memory per row: 128 threads for up
-// to 4096 keys (many rows per SM), 512 up to 16384, 1024 beyond.
+// to 4096 keys (many rows per SM), 1024 beyond (a long row's passes and rounds are its latency:
+// 1024 threads took the 64 x 8192 decode selection from 24.6 to 18.4 us, where 512 ran before;
+// more threads made the 2048-key rows slower).
 template <template <int, bool> class K, bool kBf16, class... Args>
 cudaError_t launch_rows(int keys, int64_t rows, cudaStream_t stream, Args... args) {
     const size_t smem = (size_t)keys * sizeof(uint32_t);
@@ -244,7 +246,6 @@ cudaError_t launch_rows(int keys, int64_t rows, cudaStream_t stream, Args... arg
         return cudaGetLastError();
     };
     if (keys <= 4096) return go(K<128, kBf16>::fn, 128);
-    if (keys <= 16384) return go(K<512, kBf16>::fn, 512);
     return go(K<1024, kBf16>::fn, 1024);
 }
 
