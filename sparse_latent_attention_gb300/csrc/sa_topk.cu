@@ -233,8 +233,12 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
 // to 4096 keys (many rows per SM), 1024 beyond (a long row's passes and rounds are its latency:
 // 1024 threads took the 64 x 8192 decode selection from 24.6 to 18.4 us, where 512 ran before;
 // more threads made the 2048-key rows slower).
+// The same with the thread count chosen by `span`, the positions a row's threads read (the
+// candidate blocks' threads read every position for the block maxima, then select among the far
+// fewer block keys: 1024 threads for 8192 or 32768 positions took them from 16.4 / 52.3 to
+// 12.3 / 30.7 us).
 template <template <int, bool> class K, bool kBf16, class... Args>
-cudaError_t launch_rows(int keys, int64_t rows, cudaStream_t stream, Args... args) {
+cudaError_t launch_rows_n(int keys, int span, int64_t rows, cudaStream_t stream, Args... args) {
     const size_t smem = (size_t)keys * sizeof(uint32_t);
     auto go = [&](auto kernel, int threads) -> cudaError_t {
         if (smem > 48 * 1024) {
@@ -245,8 +249,13 @@ cudaError_t launch_rows(int keys, int64_t rows, cudaStream_t stream, Args... arg
         kernel<<<(unsigned)rows, threads, smem, stream>>>(args...);
         return cudaGetLastError();
     };
-    if (keys <= 4096) return go(K<128, kBf16>::fn, 128);
+    if (span <= 4096) return go(K<128, kBf16>::fn, 128);
     return go(K<1024, kBf16>::fn, 1024);
+}
+
+template <template <int, bool> class K, bool kBf16, class... Args>
+cudaError_t launch_rows(int keys, int64_t rows, cudaStream_t stream, Args... args) {
+    return launch_rows_n<K, kBf16>(keys, keys, rows, stream, args...);
 }
 
 template <int kThreads, bool kBf16>
@@ -328,9 +337,9 @@ extern "C" sa_status sa_candidate_blocks(const void* logits, int score_format, i
     const int n = (int)n_comp;
     const cudaError_t e =
         score_format == SA_SCORE_BF16
-            ? launch_rows<CandK, true>((int)nb, b * s, st, logits, s, n, start_pos, ratio,
-                                       topk_blocks, block_size, mask)
-            : launch_rows<CandK, false>((int)nb, b * s, st, logits, s, n, start_pos, ratio,
-                                        topk_blocks, block_size, mask);
+            ? launch_rows_n<CandK, true>((int)nb, n, b * s, st, logits, s, n, start_pos, ratio,
+                                         topk_blocks, block_size, mask)
+            : launch_rows_n<CandK, false>((int)nb, n, b * s, st, logits, s, n, start_pos, ratio,
+                                          topk_blocks, block_size, mask);
     return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
