@@ -28,6 +28,27 @@ __device__ __forceinline__ float recip(float x) {
     return fmaf(y, fmaf(-x, y, 1.0f), y);
 }
 
+// f32 pairs (two lanes of one 64-bit register) for the packed add and multiply: each lane is the
+// same round-to-nearest operation as a scalar one.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 template <int HC>
 __global__ void __launch_bounds__(kTok)
     hc_split_sinkhorn_kernel(const float* __restrict__ mixes, int64_t n,
@@ -80,29 +101,44 @@ __global__ void __launch_bounds__(kTok)
 #pragma unroll
             for (int k = 0; k < HC; ++k) c[j][k] = c[j][k] * inv + eps;
         }
-        // a column step, then iters - 1 rounds of a row step and a column step
+        // a column step, then iters - 1 rounds of a row step and a column step, on the matrix held
+        // as pairs of columns (cp[j][q] = columns 2q, 2q + 1 of row j): a row's sum is one paired
+        // add and one add, a pair of columns' sums three paired adds, the scaling paired multiplies
+        static_assert(HC == 4, "the paired Sinkhorn rounds are written for hc = 4");
+        uint64_t cp[HC][2];
+#pragma unroll
+        for (int j = 0; j < HC; ++j) {
+            cp[j][0] = f2(c[j][0], c[j][1]);
+            cp[j][1] = f2(c[j][2], c[j][3]);
+        }
+        const uint64_t eps2 = f2(eps, eps);
 #pragma unroll 1
         for (int it = 0; it < iters; ++it) {
             if (it > 0) {
 #pragma unroll
                 for (int j = 0; j < HC; ++j) {
-                    float sum = 0.f;
-#pragma unroll
-                    for (int k = 0; k < HC; ++k) sum += c[j][k];
-                    const float inv = recip(sum + eps);
-#pragma unroll
-                    for (int k = 0; k < HC; ++k) c[j][k] *= inv;
+                    float a, b;
+                    f2_split(fadd2(cp[j][0], cp[j][1]), a, b);
+                    const float inv = recip((a + b) + eps);
+                    const uint64_t inv2 = f2(inv, inv);
+                    cp[j][0] = fmul2(cp[j][0], inv2);
+                    cp[j][1] = fmul2(cp[j][1], inv2);
                 }
             }
 #pragma unroll
-            for (int k = 0; k < HC; ++k) {
-                float sum = 0.f;
+            for (int q = 0; q < 2; ++q) {
+                const uint64_t sum = fadd2(fadd2(fadd2(cp[0][q], cp[1][q]), fadd2(cp[2][q], cp[3][q])), eps2);
+                float s0, s1;
+                f2_split(sum, s0, s1);
+                const uint64_t inv2 = f2(recip(s0), recip(s1));
 #pragma unroll
-                for (int j = 0; j < HC; ++j) sum += c[j][k];
-                const float inv = recip(sum + eps);
-#pragma unroll
-                for (int j = 0; j < HC; ++j) c[j][k] *= inv;
+                for (int j = 0; j < HC; ++j) cp[j][q] = fmul2(cp[j][q], inv2);
             }
+        }
+#pragma unroll
+        for (int j = 0; j < HC; ++j) {
+            f2_split(cp[j][0], c[j][0], c[j][1]);
+            f2_split(cp[j][1], c[j][2], c[j][3]);
         }
     }
     __syncthreads();  // every row has been read: the buffer now takes the outputs
