@@ -58,7 +58,8 @@ CASES = [
     (3, 1, 40, 4, 1, 0, "ties", False),              # k = 1
     (1, 257, 0, 1, 100, 0, "normal", False),         # ratio 1
     (2, 1, 16383, 4, 700, 9, "ties", True),          # 4096 positions: 128-thread block
-    (2, 1, 16387, 4, 700, 9, "ties", True),          # 4097: 512-thread block
+    (2, 1, 16387, 4, 700, 9, "ties", True),          # 4097: the shortest 1024-thread row
+    (4, 1, 32767, 4, 1024, 128, "normal", False),    # the decode shape's 8192 positions
     (2, 1, 65539, 4, 3000, 9, "normal", False),      # 16385: 1024-thread block
     (2, 1, 4 * 49152 - 1, 4, 2048, 128, "ties", False),  # the largest row (192 KB of keys)
 ]
@@ -117,6 +118,8 @@ CAND_CASES = [
     (1, 8192, 0, 4, 2048, 8, "normal", False),      # the page's 2048 x 8 over a 2048-position prefill
     (1, 8192, 0, 4, 64, 8, "normal", False),        # 64 of 256 blocks
     (64, 1, 131071, 4, 2048, 8, "normal", False),   # long decode: 4096 blocks, half kept
+    (4, 1, 32767, 4, 256, 8, "ties", True),         # 8192 positions (1024 threads), 1024 blocks
+    (2, 1, 16387, 4, 300, 8, "normal", False),      # 4097 positions: the shortest 1024-thread row
     (1, 1000, 0, 4, 16, 8, "ties", True),           # bf16, heavy ties between block maxima
     (2, 301, 0, 4, 5, 7, "specials", False),        # -0/+0/-inf, equal rows, a ragged last block
     (1, 64, 0, 4, 0, 8, "normal", False),           # no block wanted: all zeros
