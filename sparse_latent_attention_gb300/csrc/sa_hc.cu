@@ -49,6 +49,23 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
     return r;
 }
 
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// recip() of both lanes: the two approximations, then the Newton-Raphson step in pairs.
+__device__ __forceinline__ uint64_t recip2(uint64_t x) {
+    float a, b, ya, yb;
+    f2_split(x, a, b);
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(ya) : "f"(a));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(yb) : "f"(b));
+    const uint64_t y = f2(ya, yb);
+    const uint64_t e = ffma2(fmul2(x, f2(-1.f, -1.f)), y, f2(1.f, 1.f));  // 1 - x y (exact product)
+    return ffma2(y, e, y);
+}
+
 template <int HC>
 __global__ void __launch_bounds__(kTok)
     hc_split_sinkhorn_kernel(const float* __restrict__ mixes, int64_t n,
@@ -116,21 +133,23 @@ __global__ void __launch_bounds__(kTok)
         for (int it = 0; it < iters; ++it) {
             if (it > 0) {
 #pragma unroll
-                for (int j = 0; j < HC; ++j) {
-                    float a, b;
-                    f2_split(fadd2(cp[j][0], cp[j][1]), a, b);
-                    const float inv = recip((a + b) + eps);
-                    const uint64_t inv2 = f2(inv, inv);
-                    cp[j][0] = fmul2(cp[j][0], inv2);
-                    cp[j][1] = fmul2(cp[j][1], inv2);
+                for (int j = 0; j < HC; j += 2) {  // two rows' sums and reciprocals in a pair
+                    float a0, b0, a1, b1;
+                    f2_split(fadd2(cp[j][0], cp[j][1]), a0, b0);
+                    f2_split(fadd2(cp[j + 1][0], cp[j + 1][1]), a1, b1);
+                    float i0, i1;
+                    f2_split(recip2(fadd2(f2(a0 + b0, a1 + b1), eps2)), i0, i1);
+                    const uint64_t inv0 = f2(i0, i0), inv1 = f2(i1, i1);
+                    cp[j][0] = fmul2(cp[j][0], inv0);
+                    cp[j][1] = fmul2(cp[j][1], inv0);
+                    cp[j + 1][0] = fmul2(cp[j + 1][0], inv1);
+                    cp[j + 1][1] = fmul2(cp[j + 1][1], inv1);
                 }
             }
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const uint64_t sum = fadd2(fadd2(fadd2(cp[0][q], cp[1][q]), fadd2(cp[2][q], cp[3][q])), eps2);
-                float s0, s1;
-                f2_split(sum, s0, s1);
-                const uint64_t inv2 = f2(recip(s0), recip(s1));
+                const uint64_t inv2 = recip2(sum);
 #pragma unroll
                 for (int j = 0; j < HC; ++j) cp[j][q] = fmul2(cp[j][q], inv2);
             }
